@@ -1,0 +1,127 @@
+/*
+ * mla_mxfp4.h — C ABI of the GB300 (sm_103a) MXFP4 MLA decode-attention library
+ * (libmla_mxfp4.so).
+ *
+ * Operation (single-token decode, DeepSeek-style absorbed multi-head latent
+ * attention with one shared KV head stored as MXFP4).  Defined by the
+ * kernelindex "amd-mixed-mla" submissions: tensor contract and input checks in
+ * 608791 ("check_mla_inputs", "mla_decode_forward"), the MXFP4 element/scale
+ * decode in 608791 (kFp4Lut, e8m0_to_float, unpack_mxfp4) and 717900
+ * ("_nibble_to_f32"), the attention itself in 676098 ("_naive_fallback",
+ * "_mla_fused_decode_kernel") and the split-KV log-sum-exp merge in 608791
+ * ("mla_reduce_v1_like_kernel") and 676098 ("_mla_reduce_kernel"):
+ *
+ *   K[t][d] = e2m1(kv_packed[t][d/2] nibble) * 2^(kv_scale[t][d/32] - 127), d < 576
+ *   V[t][d] = K[t][d]                                                       d < 512
+ *   out[b][h][:] = sum_t softmax_t(sm_scale * q[b][h] . K[t]) V[t],
+ *                  t over rows [kv_indptr[b], kv_indptr[b+1])
+ *
+ * Layouts (all row-major, contiguous):
+ *   q          bf16  [batch][16][576]   (query row b is sequence b: one query token per sequence)
+ *   kv_packed  uint8 [rows][288]        byte j = element 2j (bits 3..0) | element 2j+1 (bits 7..4)
+ *   kv_scale   uint8 [rows][18]         E8M0; byte 0xFF is NaN, byte 0 is 2^-127
+ *   kv_indptr  int32 [batch+1]          device memory; rows used are [kv_indptr[0], kv_indptr[batch])
+ *   out        bf16  [batch][16][512]   written for every b (an empty sequence gives zeros)
+ * Buffers must hold at least kv_indptr[batch] rows.  q, kv_packed and out must be
+ * 16-byte aligned, kv_indptr 4-byte aligned; kv_scale has no alignment rule.
+ * out must not alias any input.  kv_packed and kv_scale may be NULL when there are
+ * no KV rows; the device then treats every sequence as empty (zero output) and
+ * flags MLA_DEVICE_BAD_INDPTR if kv_indptr claims rows.
+ *
+ * Every pointer argument is a DEVICE pointer on the current CUDA device, owned
+ * by the caller.  Calls are asynchronous on `stream` (no host synchronisation,
+ * no host reads of device data, no CPU fallback).  The result matches the fp64
+ * definition above to |err| <= 2e-2 + 2e-2*|ref| per element (in practice far
+ * tighter; see the test suite).
+ *
+ * Error behaviour: functions return an mla_status code.  Argument errors are
+ * detected on the host before anything is launched.  A malformed kv_indptr
+ * (negative entries, entries above kv_indptr[batch], or decreasing) cannot be
+ * seen by the host without a synchronisation, so the device clamps it into a
+ * non-decreasing sequence within [0, kv_indptr[batch]] (every access stays
+ * inside the documented buffers) and raises MLA_DEVICE_BAD_INDPTR in the device
+ * status word, readable with mla_decode_mxfp4_device_status().
+ */
+#ifndef MLA_MXFP4_H
+#define MLA_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; identical to cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st* mla_stream_t;
+
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_NULL_PTR = 1,   /* q, kv_indptr or out is NULL (batch > 0)              */
+  MLA_ERR_BAD_BATCH = 2,  /* batch < 0                                             */
+  MLA_ERR_BAD_ALIGN = 3,  /* q / kv_packed / out not 16-byte, kv_indptr not 4-byte */
+  MLA_ERR_BAD_SCALE = 4,  /* sm_scale is not finite                                */
+  MLA_ERR_WORKSPACE = 5,  /* workspace too small, or would have to grow during
+                             stream capture                                        */
+  MLA_ERR_CUDA = 6        /* a CUDA runtime call or kernel launch failed           */
+};
+
+/* Bits of the device status word (OR-ed; cleared at the start of every call). */
+enum mla_device_status {
+  MLA_DEVICE_OK = 0,
+  MLA_DEVICE_BAD_INDPTR = 1, /* kv_indptr malformed (see above); clamped               */
+  MLA_DEVICE_TIMEOUT = 2     /* an internal wait hit its time limit; output invalid   */
+};
+
+/*
+ * Decode `batch` sequences (see top of file).  batch == 0 is a no-op returning
+ * MLA_OK.  Uses a per-device workspace owned by the library, created or grown on
+ * demand with cudaMalloc (which synchronises the device); it never grows while
+ * `stream` is capturing (returns MLA_ERR_WORKSPACE instead), so capture a graph
+ * only after one eager call of at least the same batch size, or use
+ * mla_decode_mxfp4_ws.  Calls that share this workspace must be ordered (same
+ * stream, or synchronised); concurrent streams should use mla_decode_mxfp4_ws.
+ */
+int mla_decode_mxfp4(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                     const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                     mla_stream_t stream);
+
+/* Bytes of device workspace mla_decode_mxfp4_ws needs for `batch` sequences on
+ * CUDA device `device` (host-computable upper bound; 0 on error). */
+size_t mla_decode_mxfp4_workspace_bytes(int batch, int device);
+
+/* Same as mla_decode_mxfp4 but with a caller-owned device workspace of `ws_bytes`
+ * bytes (at least mla_decode_mxfp4_workspace_bytes(batch, device), 256-byte
+ * aligned).  Allocates nothing; safe to capture in a CUDA graph.  The workspace
+ * must not be used by another call that may run concurrently. */
+int mla_decode_mxfp4_ws(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                        const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                        mla_stream_t stream, void* workspace, size_t ws_bytes);
+
+/* Profiling variant of mla_decode_mxfp4_ws: additionally records `ev_split_begin`
+ * and `ev_split_end` (cudaEvent_t handles, either may be NULL) on `stream`
+ * immediately before and after the split-KV attention kernel, so that the
+ * caller can time the dominant kernel alone with cudaEventElapsedTime.  Same
+ * arguments, ownership and errors as mla_decode_mxfp4_ws. */
+int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                              const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                              mla_stream_t stream, void* workspace, size_t ws_bytes,
+                              void* ev_split_begin, void* ev_split_end);
+
+/* Debug: synchronise `stream`, then read the device status word (mla_device_status
+ * bits) left by the last call that used `workspace` (NULL = the library workspace
+ * of the current device).  Returns MLA_OK or MLA_ERR_CUDA. */
+int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, int* status);
+
+/* Free the library-owned workspaces of every device (synchronises each device
+ * that had one).  Safe to call at any time when no call is in flight. */
+void mla_decode_mxfp4_release(void);
+
+/* Human-readable name of an mla_status code. */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_MXFP4_H */

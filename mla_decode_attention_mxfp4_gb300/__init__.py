@@ -1,0 +1,12 @@
+"""GB300-native (sm_103a) MXFP4 MLA decode attention.
+
+Public API:
+  decode(q, kv_packed, kv_scale, kv_indptr, sm_scale, out=None, stream=None, workspace=None)
+  alloc_workspace(batch), workspace_bytes(batch), device_status(), HostDecoder
+and the raw C ABI mirrored in ``_lib`` (same names as include/mla_mxfp4.h).
+"""
+from .api import HostDecoder, alloc_workspace, decode, device_status, workspace_bytes  # noqa: F401
+from .build import LIB_PATH  # noqa: F401
+from .build import build as build_library  # noqa: F401
+
+SM_SCALE = 1.0 / 24.0  # 1/sqrt(576)

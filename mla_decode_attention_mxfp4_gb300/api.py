@@ -1,0 +1,119 @@
+"""PyTorch-facing wrapper of the C ABI (tensor checks + pointer marshalling).
+
+Tensor contract (kernelindex amd-mixed-mla 608791, "check_mla_inputs"):
+  q          bf16  [batch, 16, 576]   CUDA, contiguous
+  kv_packed  uint8 [rows, 288]        (or [rows, 1, 288]) CUDA, contiguous
+  kv_scale   uint8 [rows, 18]         CUDA, contiguous
+  kv_indptr  int32 [batch + 1]        CUDA, contiguous, non-decreasing
+returns      bf16  [batch, 16, 512]
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+NUM_HEADS, QK_DIM, V_DIM, PACKED, NSCALE = 16, 576, 512, 288, 18
+
+
+def _check(q, kv_packed, kv_scale, kv_indptr):
+    for name, t in (("q", q), ("kv_packed", kv_packed), ("kv_scale", kv_scale), ("kv_indptr", kv_indptr)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[1] != NUM_HEADS or q.shape[2] != QK_DIM:
+        raise ValueError("q must be bf16 [batch, 16, 576]")
+    if kv_packed.dtype != torch.uint8 or kv_packed.shape[-1] != PACKED or kv_packed.numel() % PACKED:
+        raise ValueError("kv_packed must be uint8 [rows, 288] (packed fp4x2)")
+    if kv_scale.dtype != torch.uint8 or kv_scale.shape[-1] != NSCALE:
+        raise ValueError("kv_scale must be uint8 [rows, 18] (E8M0)")
+    if kv_scale.numel() // NSCALE != kv_packed.numel() // PACKED:
+        raise ValueError("kv_scale row count must match kv_packed")
+    if kv_indptr.dtype != torch.int32 or kv_indptr.dim() != 1 or kv_indptr.numel() != q.shape[0] + 1:
+        raise ValueError("kv_indptr must be int32 [batch + 1]")
+    dev = q.device
+    for name, t in (("kv_packed", kv_packed), ("kv_scale", kv_scale), ("kv_indptr", kv_indptr)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
+
+
+def workspace_bytes(batch: int, device=None) -> int:
+    dev = torch.device(device if device is not None else "cuda").index
+    if dev is None:
+        dev = torch.cuda.current_device()
+    return _lib.mla_decode_mxfp4_workspace_bytes(batch, dev)
+
+
+def alloc_workspace(batch: int, device=None) -> torch.Tensor:
+    """A caller-owned workspace for decode(..., workspace=...) (256-byte aligned)."""
+    n = workspace_bytes(batch, device)
+    if n == 0:
+        raise RuntimeError("could not size the workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def decode(q: torch.Tensor, kv_packed: torch.Tensor, kv_scale: torch.Tensor, kv_indptr: torch.Tensor,
+           sm_scale: float, out: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None,
+           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """MXFP4 MLA decode on the GPU; returns out bf16 [batch, 16, 512]."""
+    _check(q, kv_packed, kv_scale, kv_indptr)
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty(B, NUM_HEADS, V_DIM, dtype=torch.bfloat16, device=q.device)
+    elif (out.dtype != torch.bfloat16 or tuple(out.shape) != (B, NUM_HEADS, V_DIM) or not out.is_contiguous()
+          or out.device != q.device):
+        raise ValueError("out must be contiguous bf16 [batch, 16, 512] on q's device")
+    with torch.cuda.device(q.device):
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        args = (q.data_ptr(), kv_packed.data_ptr(), kv_scale.data_ptr(), kv_indptr.data_ptr(), out.data_ptr(),
+                B, float(sm_scale), s.cuda_stream)
+        if workspace is None:
+            rc = _lib.mla_decode_mxfp4(*args)
+        else:
+            if workspace.device != q.device or not workspace.is_contiguous():
+                raise ValueError("workspace must be a contiguous tensor on q's device")
+            rc = _lib.mla_decode_mxfp4_ws(*args, workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if rc != _lib.MLA_OK:
+        raise _lib.MlaError(rc, "mla_decode_mxfp4")
+    return out
+
+
+def device_status(stream: torch.cuda.Stream | None = None, workspace: torch.Tensor | None = None) -> int:
+    """Synchronise and read the device status bits of the last call (see mla_device_status)."""
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    return _lib.mla_decode_mxfp4_device_status(s, workspace.data_ptr() if workspace is not None else None)
+
+
+class HostDecoder:
+    """End-to-end decode from pinned host buffers: H2D copies, decode, D2H of the output.
+
+    Device buffers are allocated once for the largest shape seen; each call issues
+    one copy per input, the decode kernels, and one copy back, on `stream`.
+    """
+
+    def __init__(self, device="cuda"):
+        self.device = torch.device(device)
+        self.stream = torch.cuda.Stream(self.device)
+        self._bufs = {}
+
+    def _buf(self, name, like: torch.Tensor):
+        b = self._bufs.get(name)
+        if b is None or b.numel() < like.numel() or b.dtype != like.dtype:
+            b = torch.empty(like.numel(), dtype=like.dtype, device=self.device)
+            self._bufs[name] = b
+        return b[: like.numel()].view(like.shape)
+
+    def __call__(self, q, kv_packed, kv_scale, kv_indptr, sm_scale, out_host: torch.Tensor) -> torch.Tensor:
+        with torch.cuda.stream(self.stream):
+            dq = self._buf("q", q).copy_(q, non_blocking=True)
+            dkv = self._buf("kv", kv_packed).copy_(kv_packed, non_blocking=True)
+            dsc = self._buf("sc", kv_scale).copy_(kv_scale, non_blocking=True)
+            dip = self._buf("ip", kv_indptr).copy_(kv_indptr, non_blocking=True)
+            dout = self._buf("out", out_host)
+            decode(dq, dkv, dsc, dip, sm_scale, out=dout, stream=self.stream)
+            out_host.copy_(dout, non_blocking=True)
+        return out_host
+
+    def synchronize(self):
+        self.stream.synchronize()

@@ -1,0 +1,147 @@
+"""CPU mirror of the device-side work partition and tile walk.
+
+Re-derives, in Python, what mla_partition_kernel and mla_split_kernel's tile
+iterator compute, and checks the invariants every launch relies on: every
+token row is visited exactly once, all reads stay inside [0, kv_indptr[batch])
+rows and inside the caller's scale bytes, every smem copy fits its stage, and
+partial slots are unique and below the workspace bound of 2 slots per CTA.
+"""
+import random
+
+import pytest
+
+TILE, PACKED, NSCALE, MIN_PER = 128, 288, 18, 64
+STAGE_SCALE_BYTES = 2432
+
+
+def partition(indptr, G, kv_null=False):
+    B = len(indptr) - 1
+    hi = 0 if kv_null else max(indptr[B], 0)
+    ipc, pm, bad = [], None, False
+    for i, v in enumerate(indptr):
+        if v < 0 or v > hi or (i > 0 and v < indptr[i - 1]):
+            bad = True
+        pm = v if pm is None else max(pm, v)
+        ipc.append(min(max(pm, 0), hi))
+    N = ipc[B] - ipc[0]
+    per = max(MIN_PER, -(-N // G))
+    geff = -(-N // per) if N > 0 else 0
+    seqinfo, run = [], 0
+    for b in range(B):
+        a0, a1 = ipc[b], ipc[b + 1]
+        if a1 > a0:
+            f, l = (a0 - ipc[0]) // per, (a1 - 1 - ipc[0]) // per
+        else:
+            f, l = 0, -1
+        ns = l - f + 1
+        seqinfo.append((f, l, run))
+        run += ns if ns >= 2 else 0
+    cta_first = []
+    for g in range(geff):
+        r0 = ipc[0] + g * per
+        cta_first.append(max(b for b in range(B) if ipc[b] <= r0))
+    return ipc, per, geff, seqinfo, run, cta_first, bad
+
+
+def tiles(ipc, B, g, per, first_seq):
+    rend = ipc[B]
+    r0 = ipc[0] + g * per
+    if r0 >= rend:
+        return []
+    r1 = min(rend, r0 + per)
+    b = first_seq
+    t0 = max(r0, ipc[b])
+    s1 = min(r1, ipc[b + 1])
+    out, seg, first = [], 0, True
+    while True:
+        n = min(TILE, s1 - t0)
+        assert n > 0
+        out.append((b, seg, t0, n, first, t0 + n >= s1))
+        if t0 + n < s1:
+            t0 += n
+            first = False
+            continue
+        b += 1
+        while b < B and ipc[b] == ipc[b + 1]:
+            b += 1
+        if b >= B or ipc[b] >= r1:
+            return out
+        t0, s1, seg, first = ipc[b], min(r1, ipc[b + 1]), seg + 1, True
+
+
+def check(indptr, G=152, kv_null=False):
+    B = len(indptr) - 1
+    ipc, per, geff, seqinfo, slots, cta_first, bad = partition(indptr, G, kv_null)
+    rows_limit = 0 if kv_null else max(indptr[B], 0)  # caller guarantees indptr[batch] rows
+    assert all(ipc[i] <= ipc[i + 1] for i in range(B))
+    assert geff <= G and slots <= 2 * G
+    seen = set()
+    used_slots = set()
+    scale_end = ipc[B] * NSCALE
+    for g in range(geff):
+        tl = tiles(ipc, B, g, per, cta_first[g])
+        assert tl, g
+        for (b, seg, t0, n, first, last) in tl:
+            assert 0 <= ipc[b] <= t0 and t0 + n <= ipc[b + 1] <= rows_limit
+            assert 1 <= n <= TILE
+            for r in range(t0, t0 + n):
+                assert r not in seen
+                seen.add(r)
+            # scale bytes: aligned superset by bulk copy, clamped, tail by plain loads
+            b0, b1 = t0 * NSCALE, (t0 + n) * NSCALE
+            a0 = b0 & ~15
+            a1 = min((b1 + 15) & ~15, scale_end & ~15)
+            if a1 > a0:
+                assert a1 <= scale_end and (a1 - a0) % 16 == 0 and a0 % 16 == 0
+            assert b1 - a0 <= STAGE_SCALE_BYTES
+            if last:
+                f, l, base = seqinfo[b]
+                if f != l:
+                    slot = base + (g - f)
+                    assert slot not in used_slots and 0 <= slot < 2 * G
+                    used_slots.add(slot)
+    assert sorted(seen) == list(range(ipc[0], ipc[B]))
+    for b in range(B):
+        f, l, base = seqinfo[b]
+        if l > f:
+            assert all(base + i in used_slots for i in range(l - f + 1))
+    return bad
+
+
+@pytest.mark.parametrize("G", [1, 2, 152, 304])
+def test_partition_covers_every_row_once(G):
+    rng = random.Random(G)
+    cases = [
+        [0, 256], [0, 1024, 2048, 3072, 4096], [0, 0, 0], [0, 1], [0, 0, 5, 5, 6],
+        [0] + [4096 * (i + 1) for i in range(128)],
+        [7, 7, 300, 301, 301, 900],  # non-zero base
+    ]
+    for _ in range(30):
+        B = rng.randint(1, 70)
+        lens = [rng.choice([0, 1, 2, 127, 128, 129, rng.randint(0, 40000)]) for _ in range(B)]
+        ip = [0]
+        for x in lens:
+            ip.append(ip[-1] + x)
+        cases.append(ip)
+    for ip in cases:
+        assert not check(ip, G)
+
+
+def test_ragged_workload_partition():
+    import torch
+    g = torch.Generator().manual_seed(4)
+    lens = torch.randint(1, 32769, (64,), generator=g).tolist()
+    ip = [0]
+    for x in lens:
+        ip.append(ip[-1] + x)
+    assert not check(ip, 152)
+
+
+def test_malformed_indptr_is_clamped_and_flagged():
+    for ip in ([5, 3, 10], [-4, 2, 8], [0, 10, 4, 12], [0, 50, 20]):
+        assert check(ip) is True
+
+
+def test_absent_kv_buffers_read_nothing():
+    assert check([0, 0, 0], kv_null=True) is False
+    assert check([0, 5, 9], kv_null=True) is True
