@@ -308,13 +308,14 @@ def run_native(args):
             for i in range(copies):
                 call(i)
         reps = max(1, args.steps // copies)
-        g.replay()
-        torch.cuda.synchronize(dev)
-        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ga.record(stream)
-        for _ in range(reps):
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
             g.replay()
-        gb.record(stream)
+            torch.cuda.synchronize(dev)
+            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ga.record(stream)
+            for _ in range(reps):
+                g.replay()
+            gb.record(stream)
         torch.cuda.synchronize(dev)
         graph_ms = ga.elapsed_time(gb) / (reps * copies)
     except Exception as exc:  # reported, not fatal

@@ -376,11 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           const int rem = (e2 % (kDqk / 2)) * 2;  // even slot index within the head row
           const int ks = rem >> 4, slot = rem & 15;
           const int dim = 32 * (ks >> 1) + 8 * ((slot & 7) >> 1) + 4 * (ks & 1) + 2 * (slot >> 3);
-          const float q0 = __bfloat162float(qs[h * kDqk + dim]);
-          const float q1 = __bfloat162float(qs[h * kDqk + dim + 1]);
-          const int e = eh[h];
+          // q * 2^-e as two exact power-of-two products (e in [-147, 113])
+          const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
+          const float s1 = exp2i(ea), s2 = exp2i(eb);
+          const float q0 = __bfloat162float(qs[h * kDqk + dim]) * s1 * s2;
+          const float q1 = __bfloat162float(qs[h * kDqk + dim + 1]) * s1 * s2;
           *reinterpret_cast<__half2*>(qhat + h * kQhatPitch + rem) =
-              __halves2half2(__float2half_rn(ldexpf(q0, -e)), __float2half_rn(ldexpf(q1, -e)));
+              __halves2half2(__float2half_rn(q0), __float2half_rn(q1));
         }
         named_sync(kBarQK, 128);
         if (t == 0) mbar_arrive(&bar_qempty[j & 1]);
@@ -519,9 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           }
           named_sync(kBarQK, 128);
           float* epi = reinterpret_cast<float*>(smem + kOffEpi) + (j & 1) * 48;
-          if (t < kHeads) {
-            epi[t] = lw[t] + lw[kHeads + t] + lw[2 * kHeads + t] + lw[3 * kHeads + t];
-            epi[kHeads + t] = m_run[t];
+          if (t < kHeads) epi[t] = lw[t] + lw[kHeads + t] + lw[2 * kHeads + t] + lw[3 * kHeads + t];
+          if (t == 0) {
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) epi[kHeads + h] = m_run[h];  // m_run is uniform
           }
           if (t == 0) reinterpret_cast<int*>(epi)[32] = R;
         }
