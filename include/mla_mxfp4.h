@@ -108,6 +108,31 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
                               mla_stream_t stream, void* workspace, size_t ws_bytes,
                               void* ev_split_begin, void* ev_split_end);
 
+/* No-allocation variant of mla_decode_mxfp4, for callers that may not allocate
+ * device memory at all: code running inside an allocator or memory-pool
+ * callback, processes whose device memory is fully reserved up front by a
+ * serving runtime, or hosts whose policy forbids cudaMalloc after start-up.
+ * (The pages have no counterpart; this entry point is a property of this
+ * library's C interface only.)
+ *
+ * Same arguments, layouts and results as mla_decode_mxfp4.  Instead of a
+ * workspace it uses one scratch array that the library defines statically in
+ * device memory: about 10.6 MB per GPU that loads the library, held until the
+ * process exits, sized for at most 4096 sequences per call and at most 160
+ * resident CTAs of the attention kernel (152 on GB300).  Larger requests are
+ * rejected with MLA_ERR_WORKSPACE before anything is launched.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call on a device shares the one array and it keeps
+ * the previous call's contents; nothing in it needs to start at zero (each call
+ * rewrites the metadata it reads), but calls that may overlap on the GPU (other
+ * streams, other host threads) race on it and must be ordered by the caller. */
+int mla_decode_mxfp4_noalloc(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                             const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                             mla_stream_t stream);
+
 /* Debug: synchronise `stream`, then read the device status word (mla_device_status
  * bits) left by the last call that used `workspace` (NULL = the library workspace
  * of the current device).  Returns MLA_OK or MLA_ERR_CUDA. */

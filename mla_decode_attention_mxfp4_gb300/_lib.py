@@ -93,6 +93,15 @@ def mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_
                                            stream, workspace, int(ws_bytes), ev_split_begin, ev_split_end)
 
 
+def mla_decode_mxfp4_noalloc(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream) -> int:
+    """The entry point that allocates nothing (uses the library's static device scratch)."""
+    f = lib().mla_decode_mxfp4_noalloc
+    vp = ctypes.c_void_p
+    f.restype = ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_float, vp]
+    return f(q, kv_packed, kv_scale, kv_indptr, out, int(batch), float(sm_scale), stream)
+
+
 def mla_decode_mxfp4_workspace_bytes(batch: int, device: int) -> int:
     return int(lib().mla_decode_mxfp4_workspace_bytes(int(batch), int(device)))
 

@@ -127,6 +127,25 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// ---- static scratch for callers that cannot allocate device memory ----------
+// Sized for at most kStaticMaxBatch sequences and kStaticMaxGrid resident
+// split-kernel CTAs (GB300: 152), i.e. the workspace layout of ws_offsets().
+constexpr int kStaticMaxBatch = 4096;
+constexpr int kStaticMaxGrid = 160;
+constexpr size_t static_align(size_t x) { return (x + 255) / 256 * 256; }
+constexpr size_t kStaticScratchBytes =
+    static_align(16 * sizeof(int)) + static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int)) +
+    static_align((size_t)kStaticMaxBatch * sizeof(int4)) + static_align((size_t)kStaticMaxGrid * sizeof(int)) +
+    static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * sizeof(float)) +
+    static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * mla::kDv * sizeof(float));
+
+// One copy per GPU that loads the library, alive until the process exits.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch per device (host code cannot use the
+// symbol's name as an address).  Filled on the first no-alloc call per device.
+void* g_static_ptr[kMaxDevices] = {};
+
 }  // namespace
 
 extern "C" {
@@ -200,6 +219,34 @@ int mla_decode_mxfp4(const void* q, const uint8_t* kv_packed, const uint8_t* kv_
   }
   return launch(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, reinterpret_cast<cudaStream_t>(stream), ws,
                 di);
+}
+
+int mla_decode_mxfp4_noalloc(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                             const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                             mla_stream_t stream) {
+  int rc = check_args(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale);
+  if (rc != MLA_OK || batch == 0) return rc;
+  if (batch > kStaticMaxBatch) return MLA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  DeviceInfo di;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    rc = device_info(dev, &di);
+    if (rc != MLA_OK) return rc;
+    if (di.grid > kStaticMaxGrid) return MLA_ERR_WORKSPACE;
+    if (!g_static_ptr[dev]) {
+      // set-up, once per device, with that device current
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return MLA_ERR_CUDA;
+      g_static_ptr[dev] = ptr;
+    }
+    scratch = g_static_ptr[dev];
+  }
+  if (ws_offsets(batch, di.grid).total > kStaticScratchBytes) return MLA_ERR_WORKSPACE;
+  return launch(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, reinterpret_cast<cudaStream_t>(stream),
+                scratch, di);
 }
 
 int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, int* status) {
