@@ -13,32 +13,42 @@
 //     token stream [indptr[0], indptr[B]) into G equal contiguous ranges (one per
 //     resident CTA), and records, per sequence, which ranges it touches and where
 //     its partial results go.
-//  2. mla_split_kernel (G persistent CTAs, 9 warps): each CTA walks its range in
-//     tiles of 128 tokens, one segment per sequence it overlaps.
-//       warp 8      producer: bulk async copies (packed rows, scale bytes, and the
+//  2. mla_split_kernel (G persistent CTAs): each CTA walks its range in tiles of
+//     128 tokens, one segment per sequence it overlaps.
+//       warp 16     producer: bulk async copies (packed rows, scale bytes, and the
 //                   query rows at a segment start) into a 3-stage smem ring.
-//       warps 0..3  per token: E8M0 exponents -> per-token rebased fp16 factors;
-//                   QK^T on tensor cores (mma.sync f16, fp32 accumulate) with the
-//                   e2m1 codes converted by cvt.e2m1x2; online softmax; P to smem.
-//       warps 4..7  P.V on tensor cores for 128 of the 512 V dims each; the V
-//                   fragments are built directly from packed bytes (nibble
-//                   interleave of token pairs + cvt.e2m1x2 + factor multiply).
+//       warps 0..15 token warps: warp w serves tokens 32(w%4)..+31 (its tensor-
+//                   memory lane quarter) and part w/4 of each token's work:
+//                   - E8M0 exponents -> per-token rebased fp16 factors;
+//                   - K tile (fp16, cvt.e2m1x2 + factor) -> tensor memory, and
+//                     S^T = K . Qhat^T on tcgen05 (kind::f16, A from tensor memory);
+//                   - V tile (dims 0..511) read back from tensor memory and
+//                     stored as e4m3 into shared memory (MN-major);
+//                   - online softmax; P split into e4m3 hi + lo parts (stacked as
+//                     N = 32) and O^T += V^T . P^T on tcgen05 (kind::f8f6f4) into a
+//                     tensor-memory accumulator; the P.V of tile k overlaps the
+//                     K-tile work of tile k+1.
 //     A segment that is a whole sequence writes bf16 output directly; otherwise
 //     it writes a normalised fp32 partial and its log2-sum-exp.
 //  3. mla_merge_kernel (one CTA per sequence): merges the partials of split
 //     sequences with weights 2^(lse_s - max lse); empty sequences get zeros.
 //
-// Numerics: K/V elements are formed exactly in fp16 as e2m1 * 2^(s_tb - S_t),
-// S_t the largest scale exponent of token t (exact unless a token's blocks span
-// more than 2^23); the token factor 2^(S_t - 127) is applied to the fp32 score
-// and, rebased against the running maximum R of S_t, to P before P.V.  Q is
-// carried in fp16 with a per-head power-of-two prescale (exact for |q| within
-// 2^-28 of the head's largest |q|).  Accumulation, softmax and merge are fp32.
+// Numerics: K elements are formed exactly in fp16 as e2m1 * 2^(s_tb - S_t), S_t
+// the largest scale exponent of token t (exact unless a token's blocks span more
+// than 2^23); the token factor 2^(S_t - 127) multiplies the fp32 score.  Q is
+// carried in fp16 with a per-head power-of-two prescale.  V uses the same values
+// in e4m3, exact when a token's 16 V-block exponents lie within 8 of S_t (smaller
+// blocks lose precision relative to the token's largest block).  P is rebased
+// against a running maximum that is only raised when the tile maximum exceeds it
+// by more than 2^4 (scores) or 2^4 (token exponents), so P * 2^(S_t - R) <= 256
+// fits e4m3; it is carried as hi + lo e4m3 parts (about 8 significant bits).
+// Scores, softmax statistics, accumulation and the merge are fp32.
 #pragma once
 #include <climits>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "ptx.cuh"
 
@@ -51,7 +61,9 @@ constexpr int kPacked = 288;   // bytes per token
 constexpr int kNScale = 18;    // scale bytes per token
 constexpr int kTile = 128;     // tokens per tile
 constexpr int kStages = 3;
-constexpr int kThreads = 288;  // 4 QK warps + 4 PV warps + 1 producer warp
+constexpr int kTokWarps = 16;  // 4 per tensor-memory lane quarter
+constexpr int kTokThreads = kTokWarps * 32;
+constexpr int kThreads = kTokThreads + 32;  // + 1 producer warp
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 
 constexpr int kDeviceBadIndptr = 1;
@@ -69,34 +81,44 @@ struct Workspace {
   float* part_acc;    // [2G][16][512] normalised partial output
 };
 
-// ---- shared-memory map of mla_split_kernel -----------------------------------
+// ---- shared-memory and tensor-memory map of mla_split_kernel ---------------
 constexpr int kStagePackedBytes = kTile * kPacked;                   // 36864
 constexpr int kStageScaleBytes = 2432;                               // >= 128*18 + 32, mult of 16
 constexpr int kStageBytes = kStagePackedBytes + kStageScaleBytes;    // 39296
-constexpr int kQBytes = kHeads * kDqk * 2;                           // 18432 (bf16 rows)
-constexpr int kQhatPitch = 584;                                      // halves per head row (+16 B pad)
-constexpr int kFacPitch = 18;                                        // halves per token
-constexpr int kSPitch = 20;                                          // floats per token
+constexpr int kQBytes = kHeads * kDqk * 2;                           // 18432 (bf16 / fp16 Q rows)
+
+// Tensor memory (32-bit columns, lane = token of the tile / row of M):
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 0;    // 288 columns: fp16 K tile, column c = dims (2c, 2c+1)
+constexpr uint32_t kColS = 288;  // 16 columns: S^T (fp32)
+constexpr uint32_t kColO = 320;  // 128 columns: O^T, 4 blocks of 128 dims x (16 hi + 16 lo heads)
+
+// Qhat^T, fp16, K-major without swizzle: core matrix = 8 heads x 8 dims (16 B rows);
+// offset(h, d) = (d/8)*kQLbo + (h/8)*kQSbo + (h%8)*16 + (d%8)*2.
+constexpr uint32_t kQLbo = 256, kQSbo = 128;
+// V^T, e4m3, MN-major without swizzle, 4 blocks of 128 dims:
+// offset(d, t) = (d/128)*kVtBlock + (t/8)*kVtLbo + ((d%128)/16)*kVtSbo + (t%8)*16 + d%16.
+constexpr uint32_t kVtBlock = 16384, kVtLbo = 1024, kVtSbo = 128;
+// P^T, e4m3, MN-major, n = head (hi part) or 16 + head (lo part):
+// offset(n, t) = (t/8)*kPtLbo + (n/16)*kPtSbo + (t%8)*16 + n%16.
+constexpr uint32_t kPtLbo = 256, kPtSbo = 128;
+constexpr int kMaxThresh = 4;  // raise the running maxima only by more than this (log2 units)
 
 constexpr int kOffStages = 0;
 constexpr int kOffQStage = kOffStages + kStages * kStageBytes;            // 117888
-constexpr int kOffQhat = kOffQStage + 2 * kQBytes;                        // 154752
-constexpr int kOffFac = kOffQhat + kHeads * kQhatPitch * 2;               // 173440
-constexpr int kOffS = kOffFac + 2 * kTile * kFacPitch * 2;                // 182656
-constexpr int kOffP = kOffS + kTile * kSPitch * 4;                        // 192896
-constexpr int kOffResc = kOffP + 2 * kTile * kHeads * 2;                  // 201088
-constexpr int kOffEpi = kOffResc + 2 * kHeads * 4;                        // 201216
-constexpr int kOffHmax = kOffEpi + 2 * 48 * 4;                            // 201600
-constexpr int kOffRw = kOffHmax + 4 * kHeads * 4;                         // 201856
-constexpr int kOffCh = kOffRw + 16;                                       // 201872
-constexpr int kOffLw = kOffCh + kHeads * 4;                               // 201936
-constexpr int kOffBar = kOffLw + 4 * kHeads * 4;                          // 202192
-constexpr int kSmemBytes = kOffBar + 8 * 8;                               // 202256
+constexpr int kOffQhat = kOffQStage + kQBytes;                            // 136320
+constexpr int kOffVt = kOffQhat + kQBytes;                                // 154752
+constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
+constexpr int kOffHmax = kOffPt + kTile * 32;                             // 224384
+constexpr int kOffRw = kOffHmax + 4 * kHeads * 4;                         // 224640
+constexpr int kOffCh = kOffRw + 16;                                       // 224656
+constexpr int kOffLw = kOffCh + kHeads * 4;                               // 224720
+constexpr int kOffStat = kOffLw + 4 * kHeads * 4;                         // 224976: m, alpha, resc per head
+constexpr int kOffTmem = kOffStat + 3 * kHeads * 4 + 16;                  // 225184
+constexpr int kOffBar = kOffTmem + 16;                                    // 225200
+constexpr int kSmemBytes = kOffBar + 9 * 8;                               // 225272
 
-// named barrier ids (0 is __syncthreads)
-constexpr uint32_t kBarPFull = 1;   // +parity
-constexpr uint32_t kBarPEmpty = 3;  // +parity
-constexpr uint32_t kBarQK = 5;      // QK warps only
+constexpr uint32_t kBarTok = 1;  // named barrier of the token warps
 
 struct SplitParams {
   const __nv_bfloat16* q;
@@ -269,7 +291,7 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
@@ -281,13 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_empty = bar_full + kStages;
   uint64_t* bar_qempty = bar_empty + kStages;
+  uint64_t* bar_qk = bar_qempty + 1;
+  uint64_t* bar_pv = bar_qk + 1;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 8);
+      mbar_init(&bar_empty[s], kTokWarps);
     }
-    mbar_init(&bar_qempty[0], 1);
-    mbar_init(&bar_qempty[1], 1);
+    mbar_init(bar_qempty, 1);
+    mbar_init(bar_qk, 1);
+    mbar_init(bar_pv, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -296,9 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   const bool any = it.init(p.ws.ipc, p.B, g, per, p.ws.cta_first[g]);
   if (!any) return;  // cannot happen for g < geff
   bool aborted = false;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   // =========================== producer warp ===================================
-  if (warp == 8) {
+  if (warp == kTokWarps) {
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
@@ -309,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       const int s = k % kStages;
       if (k >= kStages) wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted);
       const int j = it.seg;
-      if (it.first && j >= 2) wait_or_flag(&bar_qempty[j & 1], ((j >> 1) - 1) & 1, p, aborted);
+      if (it.first && j >= 1) wait_or_flag(bar_qempty, (j - 1) & 1, p, aborted);
       uint8_t* st = smem + kOffStages + s * kStageBytes;
       // scale bytes [18*t0, 18*(t0+n)): 16-byte aligned superset by bulk copy,
       // anything past the last aligned byte of the buffer by plain loads.
@@ -325,342 +355,315 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       bulk_g2s(st, p.kv + (long long)it.t0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
       if (a1 > a0) bulk_g2s(sdst, p.sc + a0, (uint32_t)(a1 - a0), &bar_full[s], pol_kv);
       if (it.first)
-        bulk_g2s(smem + kOffQStage + (j & 1) * kQBytes, p.q + (long long)it.b * kHeads * kDqk, kQBytes,
-                 &bar_full[s], pol_q);
+        bulk_g2s(smem + kOffQStage, p.q + (long long)it.b * kHeads * kDqk, kQBytes, &bar_full[s], pol_q);
       ++k;
     } while (it.next());
     return;
   }
 
-  __half* qhat = reinterpret_cast<__half*>(smem + kOffQhat);
+  // =========================== token warps =======================================
+  const int q4 = warp & 3, part = warp >> 2;
+  const int t = q4 * 32 + lane;  // token of the tile = tensor-memory lane
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
+  // K blocks (of 32 dims) handled by this part in pass 1: 5, 5, 4, 4
+  const int kb0 = part < 2 ? 5 * part : 10 + 4 * (part - 2);
+  const int kb1 = part < 2 ? kb0 + 5 : kb0 + 4;
+  const int h0 = 4 * part;  // heads of this part in the softmax
+  uint8_t* qhat = smem + kOffQhat;
+  uint8_t* vt = smem + kOffVt;
+  uint8_t* pt = smem + kOffPt;
   float* ch = reinterpret_cast<float*>(smem + kOffCh);
-
-  // =========================== QK / softmax warps ===============================
-  if (warp < 4) {
-    const int t = tid;  // token within the tile for per-token work
-    const int r = lane >> 2, c = lane & 3;
-    float m_run[kHeads], l_part[kHeads];
-    int R = 0;
-    int k = 0;
-    do {
-      const int s = k % kStages, par = k & 1, j = it.seg;
-      if (k >= 2) named_sync(kBarPEmpty + par, 256);
-      wait_or_flag(&bar_full[s], (k / kStages) & 1, p, aborted);
-      const uint8_t* st = smem + kOffStages + s * kStageBytes;
-      if (it.first) {
-        // ---- segment start: per-head prescale exponent and fp16 Q-hat ----
-        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage + (j & 1) * kQBytes);
-        {
-          const int h = t >> 3, part = t & 7;
-          const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + part * 72;
-          uint32_t mx = 0;
-          for (int d = 0; d < 72; ++d) mx = max(mx, (uint32_t)(qb[d] & 0x7FFFu));
-          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          if (part == 0) {
-            int e = 0;
-            if (mx != 0 && mx < 0x7F80u) {
-              int ex;
-              frexpf(__uint_as_float(mx << 16), &ex);
-              e = ex - 1 - 14;
-            }
-            reinterpret_cast<int*>(smem + kOffLw)[h] = e;
-            ch[h] = ldexpf(p.sm_scale * 1.4426950408889634f, e);
-          }
-        }
-        named_sync(kBarQK, 128);
-        const int* eh = reinterpret_cast<const int*>(smem + kOffLw);
-        for (int e2 = t; e2 < kHeads * kDqk / 2; e2 += 128) {
-          const int h = e2 / (kDqk / 2);
-          const int rem = (e2 % (kDqk / 2)) * 2;  // even slot index within the head row
-          const int ks = rem >> 4, slot = rem & 15;
-          const int dim = 32 * (ks >> 1) + 8 * ((slot & 7) >> 1) + 4 * (ks & 1) + 2 * (slot >> 3);
-          // q * 2^-e as two exact power-of-two products (e in [-147, 113])
-          const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
-          const float s1 = exp2i(ea), s2 = exp2i(eb);
-          const float q0 = __bfloat162float(qs[h * kDqk + dim]) * s1 * s2;
-          const float q1 = __bfloat162float(qs[h * kDqk + dim + 1]) * s1 * s2;
-          *reinterpret_cast<__half2*>(qhat + h * kQhatPitch + rem) =
-              __halves2half2(__float2half_rn(q0), __float2half_rn(q1));
-        }
-        named_sync(kBarQK, 128);
-        if (t == 0) mbar_arrive(&bar_qempty[j & 1]);
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          m_run[h] = -INFINITY;
-          l_part[h] = 0.f;
-        }
-        R = 0;
-      }
-      // ---- per-token scale exponents -> fp16 factors 2^(s_b - S_t) ----
-      const bool valid = t < it.n;
-      int St = 0;
-      float stok = 0.f;
+  float* hmax = reinterpret_cast<float*>(smem + kOffHmax);
+  float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [0,16) m, [16,32) alpha, [32,48) resc
+  int* flags = reinterpret_cast<int*>(smem + kOffStat + 3 * kHeads * 4);  // [0] any rescale, [1] Rnew
+  float l_part[4];
+  int R = 0;
+  bool seg_first = true;
+  int k = 0;
+  do {
+    const int s = k % kStages;
+    wait_or_flag(&bar_full[s], (k / kStages) & 1, p, aborted);
+    const uint8_t* st = smem + kOffStages + s * kStageBytes;
+    if (it.first) {
+      // ---- segment start: per-head prescale exponent and fp16 Qhat^T ----
+      // (the previous segment's QK^T MMAs, which read Qhat, completed before its softmax)
+      const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
       {
-        uint16_t* fac = reinterpret_cast<uint16_t*>(smem + kOffFac) + par * kTile * kFacPitch + t * kFacPitch;
-        const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)it.t0 * kNScale) & 15) + t * kNScale;
-        uint32_t sv[kNScale];
-        if (valid) {
-#pragma unroll
-          for (int b = 0; b < kNScale; ++b) {
-            sv[b] = sb[b];
-            St = max(St, (int)sv[b]);
+        const int h = warp;  // one head per token warp
+        const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
+        uint32_t mx = 0;
+#pragma unroll 6
+        for (int d = 0; d < 18; ++d) mx = max(mx, (uint32_t)(qb[d] & 0x7FFFu));
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+          int e = 0;
+          if (mx != 0 && mx < 0x7F80u) {
+            int ex;
+            frexpf(__uint_as_float(mx << 16), &ex);
+            e = ex - 1 - 14;
           }
-          stok = (St == 255) ? __int_as_float(0x7FC00000) : exp2i(St - 127);
-        }
-#pragma unroll
-        for (int b = 0; b < kNScale; b += 2) {
-          uint32_t lo = 0, hi = 0;
-          if (valid) {
-            lo = __half_as_ushort(__float2half_rn(exp2i((int)sv[b] - St)));
-            hi = __half_as_ushort(__float2half_rn(exp2i((int)sv[b + 1] - St)));
-          }
-          *reinterpret_cast<uint32_t*>(fac + b) = lo | (hi << 16);
+          reinterpret_cast<int*>(smem + kOffLw)[h] = e;
+          ch[h] = ldexpf(p.sm_scale * 1.4426950408889634f, e);
         }
       }
-      named_sync(kBarQK, 128);
-      // ---- S' = Qhat . (K * 2^(s - S_t)) for this warp's 32 tokens ----
-      {
-        const uint16_t* fac = reinterpret_cast<const uint16_t*>(smem + kOffFac) + par * kTile * kFacPitch;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-        const int arow = ((lane >> 3) & 1) * 8 + (lane & 7);
-        const __half* qa = qhat + arow * kQhatPitch + (lane >> 4) * 8;
-#pragma unroll 2
-        for (int b = 0; b < kNScale; ++b) {
-          uint32_t aA[4], aB[4];
-          ldsm_x4(aA, qa + (2 * b) * 16);
-          ldsm_x4(aB, qa + (2 * b + 1) * 16);
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt) {
-            const int tok = warp * 32 + nt * 8 + r;
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(st + tok * kPacked + 16 * b + 4 * c);
-            const uint32_t f = fac[tok * kFacPitch + b];
-            const uint32_t f2 = f | (f << 16);
-            uint32_t kf[4];
-            e2m1x8_to_f16x8(w, kf);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) kf[i] = hmul2_u32(kf[i], f2);
-            mma_f16_16816(acc[nt], aA, kf[0], kf[1], acc[nt]);
-            mma_f16_16816(acc[nt], aB, kf[2], kf[3], acc[nt]);
-          }
-        }
-        float* S = reinterpret_cast<float*>(smem + kOffS);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int tk = warp * 32 + nt * 8 + 2 * c;
-          S[tk * kSPitch + r] = acc[nt][0];
-          S[(tk + 1) * kSPitch + r] = acc[nt][1];
-          S[tk * kSPitch + r + 8] = acc[nt][2];
-          S[(tk + 1) * kSPitch + r + 8] = acc[nt][3];
-        }
+      named_sync(kBarTok, kTokThreads);
+      const int* eh = reinterpret_cast<const int*>(smem + kOffLw);
+      for (int e2 = tid; e2 < kHeads * kDqk / 2; e2 += kTokThreads) {
+        const int h = e2 / (kDqk / 2);
+        const int d = (e2 % (kDqk / 2)) * 2;
+        // q * 2^-e as two exact power-of-two products (e in [-147, 113])
+        const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
+        const float s1 = exp2i(ea), s2 = exp2i(eb);
+        const float q0 = __bfloat162float(qs[h * kDqk + d]) * s1 * s2;
+        const float q1 = __bfloat162float(qs[h * kDqk + d + 1]) * s1 * s2;
+        const uint32_t off = (d >> 3) * kQLbo + (h >> 3) * kQSbo + (h & 7) * 16 + (d & 7) * 2;
+        *reinterpret_cast<__half2*>(qhat + off) = __halves2half2(__float2half_rn(q0), __float2half_rn(q1));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[s]);
-      named_sync(kBarQK, 128);
-      // ---- online softmax, one token per thread ----
+      fence_proxy_async_smem();  // the tensor cores read Qhat through the async proxy
+      named_sync(kBarTok, kTokThreads);
+      if (tid == 0) mbar_arrive(bar_qempty);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) l_part[i] = 0.f;
+      R = 0;
+      seg_first = true;
+    }
+    // ---- per-token scale exponents: S_t and the factors of this part's blocks ----
+    const bool valid = t < it.n;
+    int St = 0;
+    float stok = 0.f;
+    const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)it.t0 * kNScale) & 15) + t * kNScale;
+    if (valid) {
+      // 18 bytes at an even address: nine 16-bit loads
+#pragma unroll
+      for (int i = 0; i < kNScale / 2; ++i) {
+        const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
+        St = max(St, (int)max(two & 0xFFu, two >> 8));
+      }
+      stok = (St == 255) ? __int_as_float(0x7FC00000) : exp2i(St - 127);
+    }
+    // ---- pass 1: K tile -> tensor memory (column c = dims 2c, 2c+1 of token t) ----
+    // (QK^T of the previous tile, which read this buffer, completed before its softmax;
+    // other warps of this lane quarter read it in pass 2 before the last barrier)
+    tc_fence_after();
+    {
+      const uint8_t* row = st + t * kPacked;
+#pragma unroll 1
+      for (int b = kb0; b < kb1; ++b) {
+        const uint32_t hb = valid ? (uint32_t)__half_as_ushort(__float2half_rn(exp2i((int)sb[b] - St))) : 0u;
+        const uint32_t f2 = hb | (hb << 16);
+        const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * b);
+        uint32_t v[16];
+        e2m1x8_to_f16x8(w.x, *reinterpret_cast<uint32_t(*)[4]>(&v[0]));
+        e2m1x8_to_f16x8(w.y, *reinterpret_cast<uint32_t(*)[4]>(&v[4]));
+        e2m1x8_to_f16x8(w.z, *reinterpret_cast<uint32_t(*)[4]>(&v[8]));
+        e2m1x8_to_f16x8(w.w, *reinterpret_cast<uint32_t(*)[4]>(&v[12]));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = hmul2_u32(v[i], f2);
+        tmem_st16(t_lane + kColA + 16 * b, v);
+      }
+      tc_wait_st();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_empty[s]);  // done with this stage's bytes
+    tc_fence_before();
+    named_sync(kBarTok, kTokThreads);
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_f16_f32(kTile, kHeads);
+      const uint32_t qaddr = smem_u32(qhat);
+#pragma unroll 4
+      for (int ks = 0; ks < kDqk / 16; ++ks)
+        umma_f16_ts(tmem + kColS, tmem + kColA + 8 * ks, smem_desc_kmajor(qaddr + ks * 2 * kQLbo, kQLbo, kQSbo),
+                    idesc, ks > 0 ? 1u : 0u);
+      umma_commit(bar_qk);
+    }
+    // ---- pass 2: V dims 128*part .. +127 -> e4m3 V^T block `part` in shared memory ----
+    // (P.V of the previous tile, which read V^T and P^T, must have completed)
+    if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
+    tc_fence_after();
+    {
+      uint8_t* vrow = vt + part * kVtBlock + (t >> 3) * kVtLbo + (t & 7) * 16;
+#pragma unroll
+      for (int bb = 0; bb < 4; bb += 2) {
+        const int b = 4 * part + bb;  // V block (32 dims)
+        uint32_t a[16], c[16];
+        tmem_ld16_nowait(t_lane + kColA + 16 * b, a);
+        tmem_ld16_nowait(t_lane + kColA + 16 * (b + 1), c);
+        tc_wait_ld();
+        uint8_t* d0 = vrow + 2 * bb * kVtSbo;
+        *reinterpret_cast<uint4*>(d0) = make_uint4(f16x4_to_e4m3x4(a[0], a[1]), f16x4_to_e4m3x4(a[2], a[3]),
+                                                   f16x4_to_e4m3x4(a[4], a[5]), f16x4_to_e4m3x4(a[6], a[7]));
+        *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(f16x4_to_e4m3x4(a[8], a[9]), f16x4_to_e4m3x4(a[10], a[11]),
+                                                            f16x4_to_e4m3x4(a[12], a[13]), f16x4_to_e4m3x4(a[14], a[15]));
+        *reinterpret_cast<uint4*>(d0 + 2 * kVtSbo) = make_uint4(f16x4_to_e4m3x4(c[0], c[1]), f16x4_to_e4m3x4(c[2], c[3]),
+                                                                f16x4_to_e4m3x4(c[4], c[5]), f16x4_to_e4m3x4(c[6], c[7]));
+        *reinterpret_cast<uint4*>(d0 + 3 * kVtSbo) =
+            make_uint4(f16x4_to_e4m3x4(c[8], c[9]), f16x4_to_e4m3x4(c[10], c[11]), f16x4_to_e4m3x4(c[12], c[13]),
+                       f16x4_to_e4m3x4(c[14], c[15]));
+      }
+    }
+    // ---- softmax of this tile: token t, heads h0..h0+3 ----
+    wait_or_flag(bar_qk, k & 1, p, aborted);
+    tc_fence_after();
+    float s2[4];
+    {
+      uint32_t r4[4];
+      tmem_ld4_nowait(t_lane + kColS + h0, r4);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s2[i] = valid ? __uint_as_float(r4[i]) * (ch[h0 + i] * stok) : -INFINITY;
+        const float wm = warp_max_f32(s2[i]);
+        if (lane == 0) hmax[q4 * kHeads + h0 + i] = wm;
+      }
+    }
+    const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
+    if (lane == 0 && part == 0) reinterpret_cast<int*>(smem + kOffRw)[q4] = rw;
+    named_sync(kBarTok, kTokThreads);
+    if (tid < kHeads) {
+      // per-head running statistics, computed once
+      const int h = tid;
+      const int* Rw = reinterpret_cast<const int*>(smem + kOffRw);
+      const int Rtile = max(max(Rw[0], Rw[1]), max(Rw[2], Rw[3]));
+      const int Rnew = (seg_first || Rtile > R + kMaxThresh) ? max(Rtile, seg_first ? 0 : R) : R;
+      const float rs = seg_first ? 1.f : exp2i(R - Rnew);
+      const float M = fmaxf(fmaxf(hmax[h], hmax[kHeads + h]), fmaxf(hmax[2 * kHeads + h], hmax[3 * kHeads + h]));
+      const float mo = stat[h];
+      const float mn = (seg_first || M > mo + (float)kMaxThresh) ? M : mo;
+      const float alpha = seg_first ? 0.f : ex2(mo - mn);
+      stat[h] = mn;
+      stat[kHeads + h] = alpha;
+      stat[2 * kHeads + h] = alpha * rs;
+      const bool ch_any = __any_sync(0x0000ffffu, mn != mo || Rnew != R);
+      if (h == 0) {
+        flags[0] = ch_any ? 1 : 0;
+        flags[1] = Rnew;
+      }
+    }
+    named_sync(kBarTok, kTokThreads);
+    const int Rnew = flags[1];
+    const bool any_resc = flags[0] != 0;
+    const float ptok = valid ? exp2i(St - Rnew) : 0.f;
+    uint32_t phi = 0, plo = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+      float pp[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int hh = h0 + i + u;
+        const float mn = stat[hh], alpha = stat[kHeads + hh];
+        const float pv = ex2(s2[i + u] - mn);
+        l_part[i + u] = l_part[i + u] * alpha + pv;
+        pp[u] = pv * ptok;
+      }
+      // P = hi + lo, both e4m3
+      const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pp[0], pp[1]), __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      const __nv_fp8x2_storage_t lo2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(pp[0] - hf.x, pp[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
+      phi |= (uint32_t)hi2 << (8 * i);
+      plo |= (uint32_t)lo2 << (8 * i);
+    }
+    R = Rnew;
+    {
+      uint8_t* prow = pt + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
+      *reinterpret_cast<uint32_t*>(prow) = phi;
+      *reinterpret_cast<uint32_t*>(prow + kPtSbo) = plo;
+    }
+    // ---- rescale O^T block `part` when a running maximum moved (rare) ----
+    if (!seg_first && any_resc) {
+      uint32_t a[16], c[16];
+      const uint32_t col = t_lane + kColO + 32 * part;
+      tmem_ld16_nowait(col, a);
+      tmem_ld16_nowait(col + 16, c);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float f = stat[2 * kHeads + i];
+        a[i] = __float_as_uint(__uint_as_float(a[i]) * f);
+        c[i] = __float_as_uint(__uint_as_float(c[i]) * f);
+      }
+      tmem_st16(col, a);
+      tmem_st16(col + 16, c);
+      tc_wait_st();
+    }
+    fence_proxy_async_smem();  // V^T and P^T are read by the tensor cores
+    tc_fence_before();
+    named_sync(kBarTok, kTokThreads);
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_e4m3_mn_f32(kTile, 32);
+      const uint32_t va = smem_u32(vt), pa = smem_u32(pt);
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+        for (int js = 0; js < kTile / 32; ++js)
+          umma_f8_ss(tmem + kColO + 32 * blk,
+                     smem_desc_mnmajor(va + blk * kVtBlock + js * 4 * kVtLbo, kVtLbo, kVtSbo),
+                     smem_desc_mnmajor(pa + js * 4 * kPtLbo, kPtLbo, kPtSbo), idesc,
+                     (js > 0 || !seg_first) ? 1u : 0u);
+      umma_commit(bar_pv);
+    }
+    seg_first = false;
+    if (it.last) {
+      // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
+      float* lw = reinterpret_cast<float*>(smem + kOffLw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v = l_part[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) lw[q4 * kHeads + h0 + i] = v;
+      }
+      named_sync(kBarTok, kTokThreads);
+      const float os = (R == 255) ? __int_as_float(0x7FC00000) : exp2i(R - 127);
+      const int4 si = p.ws.seqinfo[it.b];
+      const bool whole = si.x == si.y;
+      const int slot = si.z + (g - si.x);
+      if (!whole && tid < kHeads) {
+        const int h = tid;
+        const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
+        p.ws.part_lse[slot * kHeads + h] = stat[h] + lg2(L);
+      }
+      wait_or_flag(bar_pv, k & 1, p, aborted);
+      tc_fence_after();
       {
-        const float* S = reinterpret_cast<const float*>(smem + kOffS) + t * kSPitch;
-        float s2[kHeads];
-#pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-          const float4 v = *reinterpret_cast<const float4*>(S + 4 * h4);
-          s2[4 * h4 + 0] = v.x;
-          s2[4 * h4 + 1] = v.y;
-          s2[4 * h4 + 2] = v.z;
-          s2[4 * h4 + 3] = v.w;
-        }
-        float* hmax = reinterpret_cast<float*>(smem + kOffHmax);
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          s2[h] = valid ? s2[h] * (ch[h] * stok) : -INFINITY;
-          const float wm = warp_max_f32(s2[h]);
-          if (lane == 0) hmax[warp * kHeads + h] = wm;
-        }
-        const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
-        if (lane == 0) reinterpret_cast<int*>(smem + kOffRw)[warp] = rw;
-        named_sync(kBarQK, 128);
-        const int* Rw = reinterpret_cast<const int*>(smem + kOffRw);
-        const int Rnew = max(max(R, max(Rw[0], Rw[1])), max(Rw[2], Rw[3]));
-        const float rs = exp2i(R - Rnew);
-        const float ptok = valid ? exp2i(St - Rnew) : 0.f;
-        float* resc = reinterpret_cast<float*>(smem + kOffResc) + par * kHeads;
-        uint32_t ph[8];
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          const float M = fmaxf(fmaxf(hmax[h], hmax[kHeads + h]), fmaxf(hmax[2 * kHeads + h], hmax[3 * kHeads + h]));
-          const float mn = fmaxf(m_run[h], M);
-          const float alpha = ex2(m_run[h] - mn);
-          if (t == h) resc[h] = alpha * rs;
-          const float pv = ex2(s2[h] - mn);
-          l_part[h] = l_part[h] * alpha + pv;
-          m_run[h] = mn;
-          const float pp = pv * ptok;
-          if (h & 1) {
-            ph[h >> 1] |= (uint32_t)__half_as_ushort(__float2half_rn(pp)) << 16;
-          } else {
-            ph[h >> 1] = (uint32_t)__half_as_ushort(__float2half_rn(pp));
-          }
-        }
-        R = Rnew;
-        uint4* prow = reinterpret_cast<uint4*>(smem + kOffP + par * kTile * kHeads * 2 + t * 32);
-        const int sw = (t >> 2) & 1;
-        prow[sw] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        prow[sw ^ 1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-        if (it.last) {
-          float* lw = reinterpret_cast<float*>(smem + kOffLw);
-          named_sync(kBarQK, 128);  // everyone is done with eh[] (aliases lw)
+        uint32_t a[16], c[16];
+        const uint32_t col = t_lane + kColO + 32 * part;
+        tmem_ld16_nowait(col, a);
+        tmem_ld16_nowait(col + 16, c);
+        tc_wait_ld();
+        const int dim = 128 * part + t;
+        if (whole) {
+          __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
 #pragma unroll
           for (int h = 0; h < kHeads; ++h) {
-            float v = l_part[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) lw[warp * kHeads + h] = v;
+            const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
+            o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * (os / L));
           }
-          named_sync(kBarQK, 128);
-          float* epi = reinterpret_cast<float*>(smem + kOffEpi) + (j & 1) * 48;
-          if (t < kHeads) epi[t] = lw[t] + lw[kHeads + t] + lw[2 * kHeads + t] + lw[3 * kHeads + t];
-          if (t == 0) {
+        } else {
+          float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
 #pragma unroll
-            for (int h = 0; h < kHeads; ++h) epi[kHeads + h] = m_run[h];  // m_run is uniform
-          }
-          if (t == 0) reinterpret_cast<int*>(epi)[32] = R;
-        }
-      }
-      named_arrive(kBarPFull + par, 256);
-      ++k;
-    } while (it.next());
-    // match the P_EMPTY arrivals of the last two tiles
-    for (int kk = max(k - 2, 0); kk < k; ++kk) named_sync(kBarPEmpty + (kk & 1), 256);
-    return;
-  }
-
-  // =========================== P.V warps =========================================
-  {
-    const int v = warp - 4;
-    const int r = lane >> 2, c = lane & 3, n = lane >> 2;
-    float acc[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    int k = 0;
-    do {
-      const int s = k % kStages, par = k & 1, j = it.seg;
-      named_sync(kBarPFull + par, 256);
-      wait_or_flag(&bar_full[s], (k / kStages) & 1, p, aborted);
-      const uint8_t* st = smem + kOffStages + s * kStageBytes;
-      if (it.first) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-      } else {
-        const float* resc = reinterpret_cast<const float*>(smem + kOffResc) + par * kHeads;
-        const float ra = resc[r], rb = resc[r + 8];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          acc[i][0] *= ra;
-          acc[i][1] *= ra;
-          acc[i][2] *= rb;
-          acc[i][3] *= rb;
-        }
-      }
-      const uint8_t* pbase = smem + kOffP + par * kTile * kHeads * 2;
-      const uint16_t* fac = reinterpret_cast<const uint16_t*>(smem + kOffFac) + par * kTile * kFacPitch;
-      const int blkA = 4 * v + (n >> 2), blkB = blkA + 2;
-      // A-fragment row address for ldmatrix.trans: matrix mi = lane/8, row = lane%8
-      const int mi = lane >> 3, rowi = lane & 7;
-#pragma unroll 1
-      for (int ks = 0; ks < kTile / 16; ++ks) {
-        uint32_t a[4];
-        {
-          const int tok = 16 * ks + (mi >> 1) * 8 + rowi;
-          const int half = (mi & 1) ^ ((tok >> 2) & 1);
-          ldsm_x4_trans(a, pbase + tok * 32 + half * 16);
-        }
-        const int ta = 16 * ks + 2 * c;
-        uint32_t xa[2][2], ya[2][2];  // [token pair 0/1 (+8)][word A/B]
-        uint32_t fp[2][2];            // factor pairs [token pair][word A/B]
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const int t0 = ta + 8 * pr;
-          const uint8_t* row0 = st + t0 * kPacked + 64 * v + 4 * n;
-          const uint8_t* row1 = row0 + kPacked;
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(row0);
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(row1);
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(row0 + 32);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(row1 + 32);
-          xa[pr][0] = (a0 & 0x0F0F0F0Fu) | ((a1 << 4) & 0xF0F0F0F0u);
-          ya[pr][0] = ((a0 >> 4) & 0x0F0F0F0Fu) | (a1 & 0xF0F0F0F0u);
-          xa[pr][1] = (b0 & 0x0F0F0F0Fu) | ((b1 << 4) & 0xF0F0F0F0u);
-          ya[pr][1] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
-          fp[pr][0] = (uint32_t)fac[t0 * kFacPitch + blkA] | ((uint32_t)fac[(t0 + 1) * kFacPitch + blkA] << 16);
-          fp[pr][1] = (uint32_t)fac[t0 * kFacPitch + blkB] | ((uint32_t)fac[(t0 + 1) * kFacPitch + blkB] << 16);
-        }
-#pragma unroll
-        for (int wd = 0; wd < 2; ++wd) {
-          uint32_t x0[4], y0[4], x1[4], y1[4];
-          e2m1x8_to_f16x8(xa[0][wd], x0);
-          e2m1x8_to_f16x8(ya[0][wd], y0);
-          e2m1x8_to_f16x8(xa[1][wd], x1);
-          e2m1x8_to_f16x8(ya[1][wd], y1);
-#pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
-            const int jx = wd * 8 + 2 * jb, jy = jx + 1;
-            mma_f16_16816(acc[jx], a, hmul2_u32(x0[jb], fp[0][wd]), hmul2_u32(x1[jb], fp[1][wd]), acc[jx]);
-            mma_f16_16816(acc[jy], a, hmul2_u32(y0[jb], fp[0][wd]), hmul2_u32(y1[jb], fp[1][wd]), acc[jy]);
+          for (int h = 0; h < kHeads; ++h) {
+            const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
+            o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * (os / L);
           }
         }
       }
-      if (it.last) {
-        // ---- segment epilogue ----
-        const float* epi = reinterpret_cast<const float*>(smem + kOffEpi) + (j & 1) * 48;
-        const int Rf = reinterpret_cast<const int*>(epi)[32];
-        const float os = (Rf == 255) ? __int_as_float(0x7FC00000) : exp2i(Rf - 127);
-        const float sa = os / epi[r], sb = os / epi[r + 8];
-        const int4 si = p.ws.seqinfo[it.b];
-        const bool whole = si.x == si.y;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int d0 = 128 * v + 64 * half + 16 * c;
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int head = r + 8 * hh;
-            const float sc = hh ? sb : sa;
-            float vals[16];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              vals[jj] = acc[half * 8 + jj][2 * hh] * sc;
-              vals[8 + jj] = acc[half * 8 + jj][2 * hh + 1] * sc;
-            }
-            if (whole) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int q2 = 0; q2 < 8; ++q2) {
-                __nv_bfloat162 bv = __floats2bfloat162_rn(vals[2 * q2], vals[2 * q2 + 1]);
-                pk[q2] = *reinterpret_cast<uint32_t*>(&bv);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)it.b * kHeads + head) * kDv + d0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            } else {
-              const int slot = si.z + (g - si.x);
-              float4* dst = reinterpret_cast<float4*>(p.ws.part_acc + ((long long)slot * kHeads + head) * kDv + d0);
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                dst[q4] = make_float4(vals[4 * q4], vals[4 * q4 + 1], vals[4 * q4 + 2], vals[4 * q4 + 3]);
-            }
-          }
-        }
-        if (!whole && v == 0 && lane < kHeads) {
-          const int slot = si.z + (g - si.x);
-          p.ws.part_lse[slot * kHeads + lane] = epi[kHeads + lane] + lg2(epi[lane]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[s]);
-      named_arrive(kBarPEmpty + par, 256);
-      ++k;
-    } while (it.next());
+      tc_fence_before();
+      named_sync(kBarTok, kTokThreads);  // lw and the accumulator are reused by the next segment
+      tc_fence_after();
+    }
+    ++k;
+  } while (it.next());
+  // every P.V was waited for at its segment's end
+  tc_fence_before();
+  named_sync(kBarTok, kTokThreads);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
