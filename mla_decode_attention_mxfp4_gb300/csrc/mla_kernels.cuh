@@ -63,7 +63,9 @@ constexpr int kTile = 128;     // tokens per tile
 constexpr int kStages = 3;
 constexpr int kTokWarps = 16;  // 4 per tensor-memory lane quarter
 constexpr int kTokThreads = kTokWarps * 32;
-constexpr int kThreads = kTokThreads + 32;  // + 1 producer warp
+constexpr int kProdWarp = kTokWarps;      // bulk async copies
+constexpr int kMmaWarp = kTokWarps + 1;   // tcgen05.mma issue
+constexpr int kThreads = (kTokWarps + 2) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 
 constexpr int kDeviceBadIndptr = 1;
@@ -85,38 +87,43 @@ struct Workspace {
 constexpr int kStagePackedBytes = kTile * kPacked;                   // 36864
 constexpr int kStageScaleBytes = 2432;                               // >= 128*18 + 32, mult of 16
 constexpr int kStageBytes = kStagePackedBytes + kStageScaleBytes;    // 39296
-constexpr int kQBytes = kHeads * kDqk * 2;                           // 18432 (bf16 / fp16 Q rows)
+constexpr int kQBytes = kHeads * kDqk * 2;                           // 18432 (bf16 Q rows)
 
 // Tensor memory (32-bit columns, lane = token of the tile / row of M):
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0;    // 288 columns: fp16 K tile, column c = dims (2c, 2c+1)
-constexpr uint32_t kColS = 288;  // 16 columns: S^T (fp32)
-constexpr uint32_t kColO = 320;  // 128 columns: O^T, 4 blocks of 128 dims x (16 hi + 16 lo heads)
+constexpr uint32_t kColA = 0;      // 2 x 144 columns: e5m2 K tile, column c = dims 4c..4c+3
+constexpr uint32_t kColsA = 144;
+constexpr uint32_t kColS = 288;    // 2 x 32 columns: S^T from the hi (0..15) and lo (16..31) query parts
+constexpr uint32_t kColO = 384;    // 128 columns: O^T, 4 blocks of 128 dims x (16 hi + 16 lo P parts)
 
-// Qhat^T, fp16, K-major without swizzle: core matrix = 8 heads x 8 dims (16 B rows);
-// offset(h, d) = (d/8)*kQLbo + (h/8)*kQSbo + (h%8)*16 + (d%8)*2.
-constexpr uint32_t kQLbo = 256, kQSbo = 128;
-// V^T, e4m3, MN-major without swizzle, 4 blocks of 128 dims:
+// Qhat, e4m3 hi (n = head) and lo (n = 16 + head) parts, K-major without swizzle:
+// offset(n, d) = (d/16)*kQLbo + (n/8)*kQSbo + (n%8)*16 + d%16.
+constexpr uint32_t kQLbo = 512, kQSbo = 128;
+// V^T, e5m2, MN-major without swizzle, 4 blocks of 128 dims:
 // offset(d, t) = (d/128)*kVtBlock + (t/8)*kVtLbo + ((d%128)/16)*kVtSbo + (t%8)*16 + d%16.
 constexpr uint32_t kVtBlock = 16384, kVtLbo = 1024, kVtSbo = 128;
-// P^T, e4m3, MN-major, n = head (hi part) or 16 + head (lo part):
+// P^T, e4m3, MN-major, two buffers, n = head (hi part) or 16 + head (lo part):
 // offset(n, t) = (t/8)*kPtLbo + (n/16)*kPtSbo + (t%8)*16 + n%16.
-constexpr uint32_t kPtLbo = 256, kPtSbo = 128;
+constexpr uint32_t kPtLbo = 256, kPtSbo = 128, kPtBytes = kTile * 32;
 constexpr int kMaxThresh = 4;  // raise the running maxima only by more than this (log2 units)
 
 constexpr int kOffStages = 0;
 constexpr int kOffQStage = kOffStages + kStages * kStageBytes;            // 117888
 constexpr int kOffQhat = kOffQStage + kQBytes;                            // 136320
-constexpr int kOffVt = kOffQhat + kQBytes;                                // 154752
+constexpr int kOffVt = kOffQhat + 32 * kDqk;                              // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
-constexpr int kOffHmax = kOffPt + kTile * 32;                             // 224384
-constexpr int kOffRw = kOffHmax + 4 * kHeads * 4;                         // 224640
-constexpr int kOffCh = kOffRw + 16;                                       // 224656
-constexpr int kOffLw = kOffCh + kHeads * 4;                               // 224720
-constexpr int kOffStat = kOffLw + 4 * kHeads * 4;                         // 224976: m, alpha, resc per head
-constexpr int kOffTmem = kOffStat + 3 * kHeads * 4 + 16;                  // 225184
-constexpr int kOffBar = kOffTmem + 16;                                    // 225200
-constexpr int kSmemBytes = kOffBar + 9 * 8;                               // 225272
+constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480
+constexpr int kOffRw = kOffHmax + 4 * kHeads * 4;                         // 228736
+constexpr int kOffCh = kOffRw + 16;                                       // 228752: [2][16]
+constexpr int kOffEh = kOffCh + 2 * kHeads * 4;                           // 228880
+constexpr int kOffLw = kOffEh + kHeads * 4;                               // 228944
+constexpr int kOffStat = kOffLw + 4 * kHeads * 4;                         // 229200: m, alpha, resc; flags
+constexpr int kOffTmem = kOffStat + 3 * kHeads * 4 + 16;                  // 229408
+constexpr int kOffBar = kOffTmem + 16;                                    // 229424
+constexpr int kNumBars = 12;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 229520
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
 constexpr uint32_t kBarTok = 1;  // named barrier of the token warps
 
@@ -290,6 +297,96 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
   return false;
 }
 
+// Segment start: per-head prescale exponent, score factor, and the e4m3 hi/lo
+// parts of Qhat = q * 2^-E_h (two e4m3 terms hold a bf16 value exactly unless it
+// lies more than 2^11 below its head's maximum).  Called by all token threads.
+__device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int chbuf, int tid, int warp, int lane) {
+  const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
+  int* eh = reinterpret_cast<int*>(smem + kOffEh);
+  float* ch = reinterpret_cast<float*>(smem + kOffCh) + chbuf * kHeads;
+  {
+    const int h = warp;  // one head per token warp
+    const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
+    uint32_t mx = 0;
+#pragma unroll 6
+    for (int d = 0; d < 18; ++d) mx = max(mx, (uint32_t)(qb[d] & 0x7FFFu));
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+      int e = 0;
+      float f = 1.f;
+      if (mx >= 0x7F80u) {
+        f = __int_as_float(0x7FC00000);  // a non-finite query makes the head's scores NaN
+      } else if (mx != 0) {
+        int ex;
+        frexpf(__uint_as_float(mx << 16), &ex);
+        e = ex - 8;  // max |q| * 2^-e in [128, 256): below the e4m3 maximum 448
+      }
+      eh[h] = e;
+      // exact 2^e as two factors (e in [-141, 120])
+      const int ea = e / 2, eb = e - ea;
+      ch[h] = sm_scale * 1.4426950408889634f * exp2i(ea) * exp2i(eb) * f;
+    }
+  }
+  named_sync(kBarTok, kTokThreads);
+  uint8_t* qhat = smem + kOffQhat;
+  for (int e2 = tid; e2 < kHeads * kDqk / 2; e2 += kTokThreads) {
+    const int h = e2 / (kDqk / 2);
+    const int d = (e2 % (kDqk / 2)) * 2;
+    const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
+    const float s1 = exp2i(ea), s2 = exp2i(eb);
+    const float q0 = __bfloat162float(qs[h * kDqk + d]) * s1 * s2;
+    const float q1 = __bfloat162float(qs[h * kDqk + d + 1]) * s1 * s2;
+    const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_fp8x2_storage_t lo2 =
+        __nv_cvt_float2_to_fp8x2(make_float2(q0 - hf.x, q1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t off = (d >> 4) * kQLbo + (h >> 3) * kQSbo + (h & 7) * 16 + (d & 15);
+    *reinterpret_cast<uint16_t*>(qhat + off) = hi2;
+    *reinterpret_cast<uint16_t*>(qhat + off + 2 * kQSbo) = lo2;  // n = 16 + h: two 8-row groups further
+  }
+  fence_proxy_async_smem();  // the tensor cores read Qhat through the async proxy
+  named_sync(kBarTok, kTokThreads);
+}
+
+// K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
+// s_tb >= S_t - 15 (the truncated high byte of an f16 with <= 2 significant bits).
+// Token t = this thread's lane of the quarter; blocks b == part (mod 4).
+// Returns S_t (0 for tokens past the tile).
+__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane) {
+  const bool valid = t < n;
+  const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)t0 * kNScale) & 15) + t * kNScale;
+  int St = 0;
+  if (valid) {
+    // 18 bytes at an even address: nine 16-bit loads
+#pragma unroll
+    for (int i = 0; i < kNScale / 2; ++i) {
+      const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
+      St = max(St, (int)max(two & 0xFFu, two >> 8));
+    }
+  }
+  const uint8_t* row = st + t * kPacked;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const int b = part + 4 * j;
+    if (b < kNScale) {
+      const uint32_t hb = valid ? (uint32_t)__half_as_ushort(__float2half_rn(exp2i((int)sb[b] - St))) : 0u;
+      const uint32_t f2 = hb | (hb << 16);
+      const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * b);
+      uint32_t v[16];
+      e2m1x8_to_f16x8(w.x, *reinterpret_cast<uint32_t(*)[4]>(&v[0]));
+      e2m1x8_to_f16x8(w.y, *reinterpret_cast<uint32_t(*)[4]>(&v[4]));
+      e2m1x8_to_f16x8(w.z, *reinterpret_cast<uint32_t(*)[4]>(&v[8]));
+      e2m1x8_to_f16x8(w.w, *reinterpret_cast<uint32_t(*)[4]>(&v[12]));
+      uint32_t e[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) e[i] = f16x4_hi_bytes(hmul2_u32(v[2 * i], f2), hmul2_u32(v[2 * i + 1], f2));
+      tmem_st8(a_lane + 8 * b, e);
+    }
+  }
+  return St;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -300,18 +397,24 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   if (g >= geff) return;
   const int per = meta[kMetaPer];
 
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* bar_empty = bar_full + kStages;
-  uint64_t* bar_qempty = bar_empty + kStages;
-  uint64_t* bar_qk = bar_qempty + 1;
-  uint64_t* bar_pv = bar_qk + 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bar_full = bars;          // [3] stage landed (producer, tx bytes)
+  uint64_t* bar_empty = bars + 3;     // [3] stage consumed (16 token warps)
+  uint64_t* bar_qempty = bars + 6;    // query rows consumed (one per segment)
+  uint64_t* bar_kready = bars + 7;    // K tile in tensor memory and Qhat ready (16 token warps)
+  uint64_t* bar_pready = bars + 8;    // V^T, P^T and any O^T rescale done (16 token warps)
+  uint64_t* bar_qk = bars + 9;        // [2] S^T buffer written (MMA commit)
+  uint64_t* bar_pv = bars + 11;       // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], kTokWarps);
     }
     mbar_init(bar_qempty, 1);
-    mbar_init(bar_qk, 1);
+    mbar_init(bar_kready, kTokWarps);
+    mbar_init(bar_pready, kTokWarps);
+    mbar_init(&bar_qk[0], 1);
+    mbar_init(&bar_qk[1], 1);
     mbar_init(bar_pv, 1);
     fence_barrier_init();
   }
@@ -326,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
   // =========================== producer warp ===================================
-  if (warp == kTokWarps) {
+  if (warp == kProdWarp) {
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
@@ -361,159 +465,147 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     return;
   }
 
+  // =========================== MMA warp =========================================
+  // Order of issue: QK(0), then per tile k: QK(k+1) once its K tile is ready, P.V(k)
+  // once its P^T / V^T are ready.  The token warps arrive in the same order.
+  if (warp == kMmaWarp) {
+    const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
+    const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, true, true);
+    const uint64_t dq0 = smem_desc_kmajor(smem_u32(smem + kOffQhat), kQLbo, kQSbo);
+    const uint64_t dv0 = smem_desc_mnmajor(smem_u32(smem + kOffVt), kVtLbo, kVtSbo);
+    const uint64_t dp0 = smem_desc_mnmajor(smem_u32(smem + kOffPt), kPtLbo, kPtSbo);
+    TileIter cur = it, nxt = it;
+    bool has_next = nxt.next();
+    int k = 0;
+    for (int kk = 0;; ++kk) {
+      // QK^T of tile kk (kk = 0 before the loop proper, then kk = k + 1)
+      if (kk == 0 || has_next) {
+        const int q = kk;
+        wait_or_flag(bar_kready, q & 1, p, aborted);
+        tc_fence_after();
+        const uint32_t bq = q & 1;
+#pragma unroll
+        for (int ks = 0; ks < kDqk / 32; ++ks)
+          umma_f8_ts_warp(tmem + kColS + 32 * bq, tmem + kColA + kColsA * bq + 8 * ks,
+                          dq0 + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+        umma_commit_warp(&bar_qk[bq]);
+      }
+      if (kk == 0) continue;
+      // P.V of tile k
+      wait_or_flag(bar_pready, k & 1, p, aborted);
+      tc_fence_after();
+      const uint64_t dp = dp0 + (uint64_t)(((k & 1) * kPtBytes) >> 4);
+      const bool seg_first = cur.first;
+#pragma unroll
+      for (int js = 0; js < kTile / 32; ++js)
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+          umma_f8_ss_warp(tmem + kColO + 32 * blk, dv0 + (uint64_t)((blk * kVtBlock + js * 4 * kVtLbo) >> 4),
+                          dp + (uint64_t)((js * 4 * kPtLbo) >> 4), idesc_pv, (js > 0 || !seg_first) ? 1u : 0u);
+      umma_commit_warp(bar_pv);
+      if (!has_next) break;
+      cur = nxt;
+      has_next = nxt.next();
+      ++k;
+    }
+    named_sync(2, kTokThreads + 32);  // with the token warps: all issue done before dealloc
+    return;
+  }
+
   // =========================== token warps =======================================
   const int q4 = warp & 3, part = warp >> 2;
   const int t = q4 * 32 + lane;  // token of the tile = tensor-memory lane
-  const uint32_t tmem = *tmem_slot;
   const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-  // K blocks (of 32 dims) handled by this part in pass 1: 5, 5, 4, 4
-  const int kb0 = part < 2 ? 5 * part : 10 + 4 * (part - 2);
-  const int kb1 = part < 2 ? kb0 + 5 : kb0 + 4;
   const int h0 = 4 * part;  // heads of this part in the softmax
-  uint8_t* qhat = smem + kOffQhat;
   uint8_t* vt = smem + kOffVt;
-  uint8_t* pt = smem + kOffPt;
-  float* ch = reinterpret_cast<float*>(smem + kOffCh);
+  float* chs = reinterpret_cast<float*>(smem + kOffCh);
   float* hmax = reinterpret_cast<float*>(smem + kOffHmax);
   float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [0,16) m, [16,32) alpha, [32,48) resc
   int* flags = reinterpret_cast<int*>(smem + kOffStat + 3 * kHeads * 4);  // [0] any rescale, [1] Rnew
   float l_part[4];
   int R = 0;
   bool seg_first = true;
+
+  // prologue: tile 0 (a segment start)
+  wait_or_flag(&bar_full[0], 0, p, aborted);
+  build_qhat(smem, p.sm_scale, it.seg & 1, tid, warp, lane);
+  if (tid == 0) mbar_arrive(bar_qempty);
+  int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA);
+  tc_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar_kready);
+    mbar_arrive(&bar_empty[0]);
+  }
+
   int k = 0;
+  bool has_next;
   do {
-    const int s = k % kStages;
-    wait_or_flag(&bar_full[s], (k / kStages) & 1, p, aborted);
-    const uint8_t* st = smem + kOffStages + s * kStageBytes;
+    TileIter nx = it;
+    has_next = nx.next();
+    const int St = St_next;
+    const bool valid = t < it.n;
+    // ---- V^T of tile k: e5m2 bytes of V blocks b == part (mod 4) from tensor memory ----
+    // (P.V of tile k-1, which read V^T, must have completed)
+    if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
+    tc_fence_after();
+    {
+      const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
+      uint32_t e[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld8_nowait(acol + 8 * (part + 4 * j), e[j]);
+      tc_wait_ld();
+      uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int b = part + 4 * j;  // dims 32b .. 32b+31
+        uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
+        *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
+        *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
+      }
+    }
+    // ---- K tile k+1 -> tensor memory (the other buffer; QK^T of tile k-1 read it and completed) ----
+    if (has_next) {
+      const int s1 = (k + 1) % kStages;
+      wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
+      if (nx.first) {
+        // the next segment's Qhat replaces this one once QK^T of tile k has completed
+        wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
+        build_qhat(smem, p.sm_scale, nx.seg & 1, tid, warp, lane);
+        if (tid == 0) mbar_arrive(bar_qempty);
+      }
+      St_next = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, nx.t0, nx.n, t, part,
+                               t_lane + kColA + kColsA * ((k + 1) & 1));
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_kready);
+        mbar_arrive(&bar_empty[s1]);
+      }
+    }
+    // ---- softmax of tile k: token t, heads h0..h0+3 ----
     if (it.first) {
-      // ---- segment start: per-head prescale exponent and fp16 Qhat^T ----
-      // (the previous segment's QK^T MMAs, which read Qhat, completed before its softmax)
-      const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
-      {
-        const int h = warp;  // one head per token warp
-        const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
-        uint32_t mx = 0;
-#pragma unroll 6
-        for (int d = 0; d < 18; ++d) mx = max(mx, (uint32_t)(qb[d] & 0x7FFFu));
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (lane == 0) {
-          int e = 0;
-          if (mx != 0 && mx < 0x7F80u) {
-            int ex;
-            frexpf(__uint_as_float(mx << 16), &ex);
-            e = ex - 1 - 14;
-          }
-          reinterpret_cast<int*>(smem + kOffLw)[h] = e;
-          ch[h] = ldexpf(p.sm_scale * 1.4426950408889634f, e);
-        }
-      }
-      named_sync(kBarTok, kTokThreads);
-      const int* eh = reinterpret_cast<const int*>(smem + kOffLw);
-      for (int e2 = tid; e2 < kHeads * kDqk / 2; e2 += kTokThreads) {
-        const int h = e2 / (kDqk / 2);
-        const int d = (e2 % (kDqk / 2)) * 2;
-        // q * 2^-e as two exact power-of-two products (e in [-147, 113])
-        const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
-        const float s1 = exp2i(ea), s2 = exp2i(eb);
-        const float q0 = __bfloat162float(qs[h * kDqk + d]) * s1 * s2;
-        const float q1 = __bfloat162float(qs[h * kDqk + d + 1]) * s1 * s2;
-        const uint32_t off = (d >> 3) * kQLbo + (h >> 3) * kQSbo + (h & 7) * 16 + (d & 7) * 2;
-        *reinterpret_cast<__half2*>(qhat + off) = __halves2half2(__float2half_rn(q0), __float2half_rn(q1));
-      }
-      fence_proxy_async_smem();  // the tensor cores read Qhat through the async proxy
-      named_sync(kBarTok, kTokThreads);
-      if (tid == 0) mbar_arrive(bar_qempty);
 #pragma unroll
       for (int i = 0; i < 4; ++i) l_part[i] = 0.f;
       R = 0;
       seg_first = true;
     }
-    // ---- per-token scale exponents: S_t and the factors of this part's blocks ----
-    const bool valid = t < it.n;
-    int St = 0;
-    float stok = 0.f;
-    const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)it.t0 * kNScale) & 15) + t * kNScale;
-    if (valid) {
-      // 18 bytes at an even address: nine 16-bit loads
-#pragma unroll
-      for (int i = 0; i < kNScale / 2; ++i) {
-        const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
-        St = max(St, (int)max(two & 0xFFu, two >> 8));
-      }
-      stok = (St == 255) ? __int_as_float(0x7FC00000) : exp2i(St - 127);
-    }
-    // ---- pass 1: K tile -> tensor memory (column c = dims 2c, 2c+1 of token t) ----
-    // (QK^T of the previous tile, which read this buffer, completed before its softmax;
-    // other warps of this lane quarter read it in pass 2 before the last barrier)
-    tc_fence_after();
-    {
-      const uint8_t* row = st + t * kPacked;
-#pragma unroll 1
-      for (int b = kb0; b < kb1; ++b) {
-        const uint32_t hb = valid ? (uint32_t)__half_as_ushort(__float2half_rn(exp2i((int)sb[b] - St))) : 0u;
-        const uint32_t f2 = hb | (hb << 16);
-        const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * b);
-        uint32_t v[16];
-        e2m1x8_to_f16x8(w.x, *reinterpret_cast<uint32_t(*)[4]>(&v[0]));
-        e2m1x8_to_f16x8(w.y, *reinterpret_cast<uint32_t(*)[4]>(&v[4]));
-        e2m1x8_to_f16x8(w.z, *reinterpret_cast<uint32_t(*)[4]>(&v[8]));
-        e2m1x8_to_f16x8(w.w, *reinterpret_cast<uint32_t(*)[4]>(&v[12]));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = hmul2_u32(v[i], f2);
-        tmem_st16(t_lane + kColA + 16 * b, v);
-      }
-      tc_wait_st();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar_empty[s]);  // done with this stage's bytes
-    tc_fence_before();
-    named_sync(kBarTok, kTokThreads);
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_f16_f32(kTile, kHeads);
-      const uint32_t qaddr = smem_u32(qhat);
-#pragma unroll 4
-      for (int ks = 0; ks < kDqk / 16; ++ks)
-        umma_f16_ts(tmem + kColS, tmem + kColA + 8 * ks, smem_desc_kmajor(qaddr + ks * 2 * kQLbo, kQLbo, kQSbo),
-                    idesc, ks > 0 ? 1u : 0u);
-      umma_commit(bar_qk);
-    }
-    // ---- pass 2: V dims 128*part .. +127 -> e4m3 V^T block `part` in shared memory ----
-    // (P.V of the previous tile, which read V^T and P^T, must have completed)
-    if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
-    tc_fence_after();
-    {
-      uint8_t* vrow = vt + part * kVtBlock + (t >> 3) * kVtLbo + (t & 7) * 16;
-#pragma unroll
-      for (int bb = 0; bb < 4; bb += 2) {
-        const int b = 4 * part + bb;  // V block (32 dims)
-        uint32_t a[16], c[16];
-        tmem_ld16_nowait(t_lane + kColA + 16 * b, a);
-        tmem_ld16_nowait(t_lane + kColA + 16 * (b + 1), c);
-        tc_wait_ld();
-        uint8_t* d0 = vrow + 2 * bb * kVtSbo;
-        *reinterpret_cast<uint4*>(d0) = make_uint4(f16x4_to_e4m3x4(a[0], a[1]), f16x4_to_e4m3x4(a[2], a[3]),
-                                                   f16x4_to_e4m3x4(a[4], a[5]), f16x4_to_e4m3x4(a[6], a[7]));
-        *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(f16x4_to_e4m3x4(a[8], a[9]), f16x4_to_e4m3x4(a[10], a[11]),
-                                                            f16x4_to_e4m3x4(a[12], a[13]), f16x4_to_e4m3x4(a[14], a[15]));
-        *reinterpret_cast<uint4*>(d0 + 2 * kVtSbo) = make_uint4(f16x4_to_e4m3x4(c[0], c[1]), f16x4_to_e4m3x4(c[2], c[3]),
-                                                                f16x4_to_e4m3x4(c[4], c[5]), f16x4_to_e4m3x4(c[6], c[7]));
-        *reinterpret_cast<uint4*>(d0 + 3 * kVtSbo) =
-            make_uint4(f16x4_to_e4m3x4(c[8], c[9]), f16x4_to_e4m3x4(c[10], c[11]), f16x4_to_e4m3x4(c[12], c[13]),
-                       f16x4_to_e4m3x4(c[14], c[15]));
-      }
-    }
-    // ---- softmax of this tile: token t, heads h0..h0+3 ----
-    wait_or_flag(bar_qk, k & 1, p, aborted);
+    const float* ch = chs + (it.seg & 1) * kHeads;
+    const float stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
+    wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
     tc_fence_after();
     float s2[4];
     {
-      uint32_t r4[4];
-      tmem_ld4_nowait(t_lane + kColS + h0, r4);
+      uint32_t rh[4], rl[4];
+      const uint32_t scol = t_lane + kColS + 32 * (k & 1) + h0;
+      tmem_ld4_nowait(scol, rh);
+      tmem_ld4_nowait(scol + 16, rl);
       tc_wait_ld();
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        s2[i] = valid ? __uint_as_float(r4[i]) * (ch[h0 + i] * stok) : -INFINITY;
+        s2[i] = valid ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * (ch[h0 + i] * stok) : -INFINITY;
         const float wm = warp_max_f32(s2[i]);
         if (lane == 0) hmax[q4 * kHeads + h0 + i] = wm;
       }
@@ -568,11 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     }
     R = Rnew;
     {
-      uint8_t* prow = pt + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
+      uint8_t* prow = smem + kOffPt + (k & 1) * kPtBytes + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
       *reinterpret_cast<uint32_t*>(prow) = phi;
       *reinterpret_cast<uint32_t*>(prow + kPtSbo) = plo;
     }
-    // ---- rescale O^T block `part` when a running maximum moved (rare) ----
+    // ---- rescale O^T block `part` when a running maximum moved (P.V of tile k-1 is done) ----
     if (!seg_first && any_resc) {
       uint32_t a[16], c[16];
       const uint32_t col = t_lane + kColO + 32 * part;
@@ -591,21 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     }
     fence_proxy_async_smem();  // V^T and P^T are read by the tensor cores
     tc_fence_before();
-    named_sync(kBarTok, kTokThreads);
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_e4m3_mn_f32(kTile, 32);
-      const uint32_t va = smem_u32(vt), pa = smem_u32(pt);
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-        for (int js = 0; js < kTile / 32; ++js)
-          umma_f8_ss(tmem + kColO + 32 * blk,
-                     smem_desc_mnmajor(va + blk * kVtBlock + js * 4 * kVtLbo, kVtLbo, kVtSbo),
-                     smem_desc_mnmajor(pa + js * 4 * kPtLbo, kPtLbo, kPtSbo), idesc,
-                     (js > 0 || !seg_first) ? 1u : 0u);
-      umma_commit(bar_pv);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_pready);
     seg_first = false;
     if (it.last) {
       // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
@@ -654,13 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       }
       tc_fence_before();
       named_sync(kBarTok, kTokThreads);  // lw and the accumulator are reused by the next segment
-      tc_fence_after();
     }
+    it = nx;
     ++k;
-  } while (it.next());
-  // every P.V was waited for at its segment's end
+  } while (has_next);
+  // every P.V was waited for at its segment's end; the MMA warp has finished issuing
   tc_fence_before();
-  named_sync(kBarTok, kTokThreads);
+  named_sync(2, kTokThreads + 32);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
