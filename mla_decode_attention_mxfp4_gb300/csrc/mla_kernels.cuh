@@ -61,10 +61,14 @@ constexpr int kPacked = 288;   // bytes per token
 constexpr int kNScale = 18;    // scale bytes per token
 constexpr int kTile = 128;     // tokens per tile
 constexpr int kStages = 3;
-constexpr int kTokWarps = 16;  // 4 per tensor-memory lane quarter
+constexpr int kDqWarps = 16;                 // dequant group: 4 warps per tensor-memory lane quarter
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kSmWarps = 8;                  // softmax group: 2 warps per lane quarter
+constexpr int kSmThreads = kSmWarps * 32;
+constexpr int kTokWarps = kDqWarps + kSmWarps;
 constexpr int kTokThreads = kTokWarps * 32;
-constexpr int kProdWarp = kTokWarps;      // bulk async copies
-constexpr int kMmaWarp = kTokWarps + 1;   // tcgen05.mma issue
+constexpr int kProdWarp = kTokWarps;         // bulk async copies
+constexpr int kMmaWarp = kTokWarps + 1;      // tcgen05.mma issue
 constexpr int kThreads = (kTokWarps + 2) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 
@@ -112,20 +116,23 @@ constexpr int kOffQStage = kOffStages + kStages * kStageBytes;            // 117
 constexpr int kOffQhat = kOffQStage + kQBytes;                            // 136320
 constexpr int kOffVt = kOffQhat + 32 * kDqk;                              // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
-constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480
-constexpr int kOffRw = kOffHmax + 4 * kHeads * 4;                         // 228736
-constexpr int kOffCh = kOffRw + 16;                                       // 228752: [2][16]
-constexpr int kOffEh = kOffCh + 2 * kHeads * 4;                           // 228880
-constexpr int kOffLw = kOffEh + kHeads * 4;                               // 228944
-constexpr int kOffStat = kOffLw + 4 * kHeads * 4;                         // 229200: m, alpha, resc; flags
-constexpr int kOffTmem = kOffStat + 3 * kHeads * 4 + 16;                  // 229408
-constexpr int kOffBar = kOffTmem + 16;                                    // 229424
-constexpr int kNumBars = 12;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 229520
+constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][4][16] tile maxima
+constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: [2][4] token-exponent maxima
+constexpr int kOffCh = kOffRw + 32;                                       // 229024: [4][16] score factors
+constexpr int kOffEh = kOffCh + 4 * kHeads * 4;                           // 229280
+constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229344: [4][16]
+constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] m, [16] output factors
+constexpr int kOffSt = kOffMlast + 2 * kHeads * 4;                        // 229728: [2][128] token exponents
+constexpr int kOffTmem = kOffSt + 2 * kTile * 4;                          // 230752
+constexpr int kOffBar = kOffTmem + 16;                                    // 230768
+constexpr int kNumBars = 16;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 230896
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
-constexpr uint32_t kBarTok = 1;  // named barrier of the token warps
+constexpr uint32_t kBarSm = 1;     // named barrier of the softmax group
+constexpr uint32_t kBarAll = 2;    // dequant + softmax groups + MMA warp
+constexpr uint32_t kBarDq = 3;     // named barrier of the dequant group
 
 struct SplitParams {
   const __nv_bfloat16* q;
@@ -299,13 +306,14 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
 
 // Segment start: per-head prescale exponent, score factor, and the e4m3 hi/lo
 // parts of Qhat = q * 2^-E_h (two e4m3 terms hold a bf16 value exactly unless it
-// lies more than 2^11 below its head's maximum).  Called by all token threads.
-__device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int chbuf, int tid, int warp, int lane) {
+// lies more than 2^11 below its head's maximum).  Run by the dequant group
+// (gtid 0..511, one head per warp); ends with the group's barrier.
+__device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int chbuf, int gtid, int gwarp, int lane) {
   const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
   int* eh = reinterpret_cast<int*>(smem + kOffEh);
   float* ch = reinterpret_cast<float*>(smem + kOffCh) + chbuf * kHeads;
   {
-    const int h = warp;  // one head per token warp
+    const int h = gwarp;
     const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
     uint32_t mx = 0;
 #pragma unroll 6
@@ -322,14 +330,13 @@ __device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int ch
         e = ex - 8;  // max |q| * 2^-e in [128, 256): below the e4m3 maximum 448
       }
       eh[h] = e;
-      // exact 2^e as two factors (e in [-141, 120])
-      const int ea = e / 2, eb = e - ea;
+      const int ea = e / 2, eb = e - ea;  // exact 2^e as two factors (e in [-141, 120])
       ch[h] = sm_scale * 1.4426950408889634f * exp2i(ea) * exp2i(eb) * f;
     }
   }
-  named_sync(kBarTok, kTokThreads);
+  named_sync(kBarDq, kDqThreads);
   uint8_t* qhat = smem + kOffQhat;
-  for (int e2 = tid; e2 < kHeads * kDqk / 2; e2 += kTokThreads) {
+  for (int e2 = gtid; e2 < kHeads * kDqk / 2; e2 += kDqThreads) {
     const int h = e2 / (kDqk / 2);
     const int d = (e2 % (kDqk / 2)) * 2;
     const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
@@ -346,7 +353,7 @@ __device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int ch
     *reinterpret_cast<uint16_t*>(qhat + off + 2 * kQSbo) = lo2;  // n = 16 + h: two 8-row groups further
   }
   fence_proxy_async_smem();  // the tensor cores read Qhat through the async proxy
-  named_sync(kBarTok, kTokThreads);
+  named_sync(kBarDq, kDqThreads);
 }
 
 // K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
@@ -358,33 +365,73 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
   const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)t0 * kNScale) & 15) + t * kNScale;
   int St = 0;
   if (valid) {
-    // 18 bytes at an even address: nine 16-bit loads
+    // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
+    // high byte of the largest 16-bit word
+    uint32_t mhi = 0, mlo = 0;
 #pragma unroll
     for (int i = 0; i < kNScale / 2; ++i) {
       const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
-      St = max(St, (int)max(two & 0xFFu, two >> 8));
+      mhi = max(mhi, two);
+      mlo = max(mlo, two & 0xFFu);
     }
+    St = (int)max(mhi >> 8, mlo);
   }
   const uint8_t* row = st + t * kPacked;
-#pragma unroll
+#pragma unroll 2
   for (int j = 0; j < 5; ++j) {
     const int b = part + 4 * j;
     if (b < kNScale) {
-      const uint32_t hb = valid ? (uint32_t)__half_as_ushort(__float2half_rn(exp2i((int)sb[b] - St))) : 0u;
-      const uint32_t f2 = hb | (hb << 16);
       const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * b);
-      uint32_t v[16];
-      e2m1x8_to_f16x8(w.x, *reinterpret_cast<uint32_t(*)[4]>(&v[0]));
-      e2m1x8_to_f16x8(w.y, *reinterpret_cast<uint32_t(*)[4]>(&v[4]));
-      e2m1x8_to_f16x8(w.z, *reinterpret_cast<uint32_t(*)[4]>(&v[8]));
-      e2m1x8_to_f16x8(w.w, *reinterpret_cast<uint32_t(*)[4]>(&v[12]));
+      // f16 2^(s - S_t): exponent field s - S_t + 15 when normal, a subnormal bit down to 2^-24, else 0
+      uint32_t hb = 0;
+      if (valid) {
+        const int r = (int)sb[b] - St;
+        hb = r >= -14 ? (uint32_t)(r + 15) << 10 : (r >= -24 ? 1u << (r + 24) : 0u);
+      }
+      const uint32_t f2 = hb * 0x10001u;
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       uint32_t e[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) e[i] = f16x4_hi_bytes(hmul2_u32(v[2 * i], f2), hmul2_u32(v[2 * i + 1], f2));
+      for (int i = 0; i < 4; ++i) {
+        uint32_t v[4];
+        e2m1x8_to_f16x8(ws[i], v);
+        e[2 * i] = f16x4_hi_bytes(hmul2_u32(v[0], f2), hmul2_u32(v[1], f2));
+        e[2 * i + 1] = f16x4_hi_bytes(hmul2_u32(v[2], f2), hmul2_u32(v[3], f2));
+      }
       tmem_st8(a_lane + 8 * b, e);
     }
   }
   return St;
+}
+
+// Maximum (kMax) or sum over the 32 lanes of eight per-lane values; lane L ends
+// with the result for value index 4*b4 + 2*b3 + b2 (b_i = bit i of L).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float a[4], c[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? v[i] : v[i + 4], keep = b4 ? v[i + 4] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+    a[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? a[i] : a[i + 2], keep = b3 ? a[i + 2] : a[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 8);
+    c[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  float d;
+  {
+    const float send = b2 ? c[0] : c[1], keep = b2 ? c[1] : c[0];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 4);
+    d = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  const float r2 = __shfl_xor_sync(0xffffffffu, d, 2);
+  d = kMax ? fmaxf(d, r2) : d + r2;
+  const float r1 = __shfl_xor_sync(0xffffffffu, d, 1);
+  return kMax ? fmaxf(d, r1) : d + r1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
@@ -399,20 +446,26 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_full = bars;          // [3] stage landed (producer, tx bytes)
-  uint64_t* bar_empty = bars + 3;     // [3] stage consumed (16 token warps)
+  uint64_t* bar_empty = bars + 3;     // [3] stage consumed (dequant group)
   uint64_t* bar_qempty = bars + 6;    // query rows consumed (one per segment)
-  uint64_t* bar_kready = bars + 7;    // K tile in tensor memory and Qhat ready (16 token warps)
-  uint64_t* bar_pready = bars + 8;    // V^T, P^T and any O^T rescale done (16 token warps)
-  uint64_t* bar_qk = bars + 9;        // [2] S^T buffer written (MMA commit)
-  uint64_t* bar_pv = bars + 11;       // P.V of a tile completed (MMA commit)
+  uint64_t* bar_kready = bars + 7;    // [2] K tile in tensor-memory buffer b, and its Qhat, ready (dequant group)
+  uint64_t* bar_vready = bars + 9;    // V^T of a tile in shared memory (dequant group)
+  uint64_t* bar_stready = bars + 10;  // [2] token exponents of a tile published (dequant group)
+  uint64_t* bar_pready = bars + 12;   // P^T and any O^T rescale of a tile done (softmax group)
+  uint64_t* bar_qk = bars + 13;       // [2] S^T buffer b written (MMA commit)
+  uint64_t* bar_pv = bars + 15;       // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], kTokWarps);
+      mbar_init(&bar_empty[s], kDqWarps);
     }
     mbar_init(bar_qempty, 1);
-    mbar_init(bar_kready, kTokWarps);
-    mbar_init(bar_pready, kTokWarps);
+    mbar_init(&bar_kready[0], kDqWarps);
+    mbar_init(&bar_kready[1], kDqWarps);
+    mbar_init(bar_vready, kDqWarps);
+    mbar_init(&bar_stready[0], kDqWarps);
+    mbar_init(&bar_stready[1], kDqWarps);
+    mbar_init(bar_pready, kSmWarps);
     mbar_init(&bar_qk[0], 1);
     mbar_init(&bar_qk[1], 1);
     mbar_init(bar_pv, 1);
@@ -467,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 
   // =========================== MMA warp =========================================
   // Order of issue: QK(0), then per tile k: QK(k+1) once its K tile is ready, P.V(k)
-  // once its P^T / V^T are ready.  The token warps arrive in the same order.
+  // once its V^T and P^T are ready.
   if (warp == kMmaWarp) {
     const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
     const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, true, true);
@@ -481,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       // QK^T of tile kk (kk = 0 before the loop proper, then kk = k + 1)
       if (kk == 0 || has_next) {
         const int q = kk;
-        wait_or_flag(bar_kready, q & 1, p, aborted);
+        wait_or_flag(&bar_kready[q & 1], (q >> 1) & 1, p, aborted);
         tc_fence_after();
         const uint32_t bq = q & 1;
 #pragma unroll
@@ -492,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       }
       if (kk == 0) continue;
       // P.V of tile k
+      wait_or_flag(bar_vready, k & 1, p, aborted);
       wait_or_flag(bar_pready, k & 1, p, aborted);
       tc_fence_after();
       const uint64_t dp = dp0 + (uint64_t)(((k & 1) * kPtBytes) >> 4);
@@ -508,238 +562,290 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       has_next = nxt.next();
       ++k;
     }
-    named_sync(2, kTokThreads + 32);  // with the token warps: all issue done before dealloc
+    named_sync(kBarAll, kTokThreads + 32);  // all issue done before the dealloc
     return;
   }
 
-  // =========================== token warps =======================================
-  const int q4 = warp & 3, part = warp >> 2;
+  const int q4 = warp & 3;
   const int t = q4 * 32 + lane;  // token of the tile = tensor-memory lane
   const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-  const int h0 = 4 * part;  // heads of this part in the softmax
-  uint8_t* vt = smem + kOffVt;
-  float* chs = reinterpret_cast<float*>(smem + kOffCh);
-  float* hmax = reinterpret_cast<float*>(smem + kOffHmax);
-  float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [0,16) m, [16,32) alpha, [32,48) resc
-  int* flags = reinterpret_cast<int*>(smem + kOffStat + 3 * kHeads * 4);  // [0] any rescale, [1] Rnew
-  float l_part[4];
-  int R = 0;
-  bool seg_first = true;
+  int* st_buf = reinterpret_cast<int*>(smem + kOffSt);  // [2][128]
 
-  // prologue: tile 0 (a segment start)
-  wait_or_flag(&bar_full[0], 0, p, aborted);
-  build_qhat(smem, p.sm_scale, it.seg & 1, tid, warp, lane);
-  if (tid == 0) mbar_arrive(bar_qempty);
-  int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA);
-  tc_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) {
-    mbar_arrive(bar_kready);
-    mbar_arrive(&bar_empty[0]);
-  }
-
-  int k = 0;
-  bool has_next;
-  do {
-    TileIter nx = it;
-    has_next = nx.next();
-    const int St = St_next;
-    const bool valid = t < it.n;
-    // ---- V^T of tile k: e5m2 bytes of V blocks b == part (mod 4) from tensor memory ----
-    // (P.V of tile k-1, which read V^T, must have completed)
-    if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
-    tc_fence_after();
-    {
-      const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
-      uint32_t e[4][8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld8_nowait(acol + 8 * (part + 4 * j), e[j]);
-      tc_wait_ld();
-      uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int b = part + 4 * j;  // dims 32b .. 32b+31
-        uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
-        *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
-        *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
-      }
-    }
-    // ---- K tile k+1 -> tensor memory (the other buffer; QK^T of tile k-1 read it and completed) ----
-    if (has_next) {
-      const int s1 = (k + 1) % kStages;
-      wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
-      if (nx.first) {
-        // the next segment's Qhat replaces this one once QK^T of tile k has completed
-        wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
-        build_qhat(smem, p.sm_scale, nx.seg & 1, tid, warp, lane);
-        if (tid == 0) mbar_arrive(bar_qempty);
-      }
-      St_next = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, nx.t0, nx.n, t, part,
-                               t_lane + kColA + kColsA * ((k + 1) & 1));
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_kready);
-        mbar_arrive(&bar_empty[s1]);
-      }
-    }
-    // ---- softmax of tile k: token t, heads h0..h0+3 ----
-    if (it.first) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) l_part[i] = 0.f;
-      R = 0;
-      seg_first = true;
-    }
-    const float* ch = chs + (it.seg & 1) * kHeads;
-    const float stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
-    wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
-    tc_fence_after();
-    float s2[4];
-    {
-      uint32_t rh[4], rl[4];
-      const uint32_t scol = t_lane + kColS + 32 * (k & 1) + h0;
-      tmem_ld4_nowait(scol, rh);
-      tmem_ld4_nowait(scol + 16, rl);
-      tc_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s2[i] = valid ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * (ch[h0 + i] * stok) : -INFINITY;
-        const float wm = warp_max_f32(s2[i]);
-        if (lane == 0) hmax[q4 * kHeads + h0 + i] = wm;
-      }
-    }
-    const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
-    if (lane == 0 && part == 0) reinterpret_cast<int*>(smem + kOffRw)[q4] = rw;
-    named_sync(kBarTok, kTokThreads);
-    if (tid < kHeads) {
-      // per-head running statistics, computed once
-      const int h = tid;
-      const int* Rw = reinterpret_cast<const int*>(smem + kOffRw);
-      const int Rtile = max(max(Rw[0], Rw[1]), max(Rw[2], Rw[3]));
-      const int Rnew = (seg_first || Rtile > R + kMaxThresh) ? max(Rtile, seg_first ? 0 : R) : R;
-      const float rs = seg_first ? 1.f : exp2i(R - Rnew);
-      const float M = fmaxf(fmaxf(hmax[h], hmax[kHeads + h]), fmaxf(hmax[2 * kHeads + h], hmax[3 * kHeads + h]));
-      const float mo = stat[h];
-      const float mn = (seg_first || M > mo + (float)kMaxThresh) ? M : mo;
-      const float alpha = seg_first ? 0.f : ex2(mo - mn);
-      stat[h] = mn;
-      stat[kHeads + h] = alpha;
-      stat[2 * kHeads + h] = alpha * rs;
-      const bool ch_any = __any_sync(0x0000ffffu, mn != mo || Rnew != R);
-      if (h == 0) {
-        flags[0] = ch_any ? 1 : 0;
-        flags[1] = Rnew;
-      }
-    }
-    named_sync(kBarTok, kTokThreads);
-    const int Rnew = flags[1];
-    const bool any_resc = flags[0] != 0;
-    const float ptok = valid ? exp2i(St - Rnew) : 0.f;
-    uint32_t phi = 0, plo = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i += 2) {
-      float pp[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int hh = h0 + i + u;
-        const float mn = stat[hh], alpha = stat[kHeads + hh];
-        const float pv = ex2(s2[i + u] - mn);
-        l_part[i + u] = l_part[i + u] * alpha + pv;
-        pp[u] = pv * ptok;
-      }
-      // P = hi + lo, both e4m3
-      const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pp[0], pp[1]), __NV_SATFINITE, __NV_E4M3);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      const __nv_fp8x2_storage_t lo2 =
-          __nv_cvt_float2_to_fp8x2(make_float2(pp[0] - hf.x, pp[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
-      phi |= (uint32_t)hi2 << (8 * i);
-      plo |= (uint32_t)lo2 << (8 * i);
-    }
-    R = Rnew;
-    {
-      uint8_t* prow = smem + kOffPt + (k & 1) * kPtBytes + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
-      *reinterpret_cast<uint32_t*>(prow) = phi;
-      *reinterpret_cast<uint32_t*>(prow + kPtSbo) = plo;
-    }
-    // ---- rescale O^T block `part` when a running maximum moved (P.V of tile k-1 is done) ----
-    if (!seg_first && any_resc) {
-      uint32_t a[16], c[16];
-      const uint32_t col = t_lane + kColO + 32 * part;
-      tmem_ld16_nowait(col, a);
-      tmem_ld16_nowait(col + 16, c);
-      tc_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float f = stat[2 * kHeads + i];
-        a[i] = __float_as_uint(__uint_as_float(a[i]) * f);
-        c[i] = __float_as_uint(__uint_as_float(c[i]) * f);
-      }
-      tmem_st16(col, a);
-      tmem_st16(col + 16, c);
-      tc_wait_st();
-    }
-    fence_proxy_async_smem();  // V^T and P^T are read by the tensor cores
+  if (warp < kDqWarps) {
+    // ======================= dequant group (warps 0..15) ========================
+    // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
+    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod 4).
+    const int part = warp >> 2;
+    const int gtid = tid;  // 0..511
+    uint8_t* vt = smem + kOffVt;
+    // prologue: tile 0 (a segment start)
+    wait_or_flag(&bar_full[0], 0, p, aborted);
+    build_qhat(smem, p.sm_scale, it.seg & 3, gtid, warp, lane);
+    if (gtid == 0) mbar_arrive(bar_qempty);
+    int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA);
+    tc_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_pready);
-    seg_first = false;
-    if (it.last) {
-      // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
-      float* lw = reinterpret_cast<float*>(smem + kOffLw);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v = l_part[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) lw[q4 * kHeads + h0 + i] = v;
+    if (lane == 0) {
+      mbar_arrive(&bar_kready[0]);
+      mbar_arrive(&bar_empty[0]);
+    }
+    if (part == 0) st_buf[t] = St_next;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_stready[0]);
+    int k = 0;
+    bool has_next;
+    do {
+      TileIter nx = it;
+      has_next = nx.next();
+      if (has_next) {
+        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed ----
+        const int s1 = (k + 1) % kStages;
+        wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
+        if (k >= 1) wait_or_flag(&bar_qk[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
+        if (nx.first) {
+          // the next segment's Qhat replaces this one once QK^T of tile k has completed
+          wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
+          build_qhat(smem, p.sm_scale, nx.seg & 3, gtid, warp, lane);
+          if (gtid == 0) mbar_arrive(bar_qempty);
+        }
+        tc_fence_after();
+        St_next = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, nx.t0, nx.n, t, part,
+                                 t_lane + kColA + kColsA * ((k + 1) & 1));
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar_kready[(k + 1) & 1]);
+          mbar_arrive(&bar_empty[s1]);
+        }
       }
-      named_sync(kBarTok, kTokThreads);
-      const float os = (R == 255) ? __int_as_float(0x7FC00000) : exp2i(R - 127);
-      const int4 si = p.ws.seqinfo[it.b];
-      const bool whole = si.x == si.y;
-      const int slot = si.z + (g - si.x);
-      if (!whole && tid < kHeads) {
-        const int h = tid;
-        const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
-        p.ws.part_lse[slot * kHeads + h] = stat[h] + lg2(L);
-      }
-      wait_or_flag(bar_pv, k & 1, p, aborted);
+      // ---- V^T of tile k (P.V of tile k-1, which read V^T, must have completed) ----
+      if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
       tc_fence_after();
       {
-        uint32_t a[16], c[16];
-        const uint32_t col = t_lane + kColO + 32 * part;
-        tmem_ld16_nowait(col, a);
-        tmem_ld16_nowait(col + 16, c);
-        tc_wait_ld();
-        const int dim = 128 * part + t;
-        if (whole) {
-          __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
+        const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
+        uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
 #pragma unroll
-          for (int h = 0; h < kHeads; ++h) {
-            const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
-            o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * (os / L));
-          }
-        } else {
-          float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t e[2][8];
 #pragma unroll
-          for (int h = 0; h < kHeads; ++h) {
-            const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
-            o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * (os / L);
+          for (int j = 0; j < 2; ++j) tmem_ld8_nowait(acol + 8 * (part + 4 * (2 * hb + j)), e[j]);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int b = part + 4 * (2 * hb + j);  // dims 32b .. 32b+31
+            uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
+            *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
+            *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
           }
         }
       }
+      fence_proxy_async_smem();  // V^T is read by the tensor cores
       tc_fence_before();
-      named_sync(kBarTok, kTokThreads);  // lw and the accumulator are reused by the next segment
-    }
-    it = nx;
-    ++k;
-  } while (has_next);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_vready);
+      // ---- publish the token exponents of tile k+1 (the softmax of tile k-1, which used
+      // this buffer, finished before P.V of tile k-1) ----
+      if (has_next) {
+        if (part == 0) st_buf[((k + 1) & 1) * kTile + t] = St_next;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_stready[(k + 1) & 1]);
+      }
+      it = nx;
+      ++k;
+    } while (has_next);
+  } else {
+    // ======================= softmax group (warps 16..23) =======================
+    // Warp (q4, part) owns tokens 32*q4.. and heads 8*part..8*part+7 (their running
+    // statistics and O^T columns), and O^T blocks 2*part, 2*part+1 at a segment end.
+    const int part = (warp - kDqWarps) >> 2;
+    const int h0 = 8 * part;
+    const int stid = tid - kDqThreads;  // 0..255
+    const float* chs = reinterpret_cast<const float*>(smem + kOffCh);
+    float l_part[8], m_run[8];
+    int R = 0;
+    int k = 0;
+    bool has_next;
+    do {
+      TileIter nx = it;
+      has_next = nx.next();
+      const bool valid = t < it.n;
+      const bool seg_first = it.first;
+      wait_or_flag(&bar_stready[k & 1], (k >> 1) & 1, p, aborted);
+      const int St = st_buf[(k & 1) * kTile + t];
+      const float* ch = chs + (it.seg & 3) * kHeads;
+      const float stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
+      wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
+      tc_fence_after();
+      float s2[8];
+      float* hmax = reinterpret_cast<float*>(smem + kOffHmax) + (k & 1) * 4 * kHeads;
+      int* rwb = reinterpret_cast<int*>(smem + kOffRw) + (k & 1) * 4;
+      {
+        uint32_t rh[8], rl[8];
+        const uint32_t scol = t_lane + kColS + 32 * (k & 1) + h0;
+        tmem_ld8_nowait(scol, rh);
+        tmem_ld8_nowait(scol + 16, rl);
+        tc_wait_ld();
+        const float cs = stok;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          s2[i] = valid ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * (ch[h0 + i] * cs) : -INFINITY;
+        const float wm = warp_reduce8<true>(s2, lane);
+        if ((lane & 3) == 0) hmax[q4 * kHeads + h0 + (lane >> 2)] = wm;
+      }
+      const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
+      if (lane == 0 && part == 0) rwb[q4] = rw;
+      named_sync(kBarSm, kSmThreads);
+      // running statistics of this warp's heads (every lane computes the same values)
+      float alpha[8];
+      int Rnew;
+      bool resc;
+      {
+        const int4 rwv = *reinterpret_cast<const int4*>(rwb);
+        const int Rtile = max(max(rwv.x, rwv.y), max(rwv.z, rwv.w));
+        Rnew = seg_first ? Rtile : (Rtile > R + kMaxThresh ? Rtile : R);
+        resc = !seg_first && Rnew != R;
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          float M[4];
+          const float4 a0 = *reinterpret_cast<const float4*>(hmax + h0 + 4 * hv);
+          const float4 a1 = *reinterpret_cast<const float4*>(hmax + kHeads + h0 + 4 * hv);
+          const float4 a2 = *reinterpret_cast<const float4*>(hmax + 2 * kHeads + h0 + 4 * hv);
+          const float4 a3 = *reinterpret_cast<const float4*>(hmax + 3 * kHeads + h0 + 4 * hv);
+          M[0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+          M[1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+          M[2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+          M[3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 4 * hv + u;
+            if (seg_first) {
+              m_run[i] = M[u];
+              alpha[i] = 0.f;
+              l_part[i] = 0.f;
+            } else if (M[u] > m_run[i] + (float)kMaxThresh) {
+              alpha[i] = ex2(m_run[i] - M[u]);
+              m_run[i] = M[u];
+              resc = true;
+            } else {
+              alpha[i] = 1.f;
+            }
+          }
+        }
+      }
+      const float ptok = valid ? exp2i(St - Rnew) : 0.f;
+      uint32_t phi[2] = {0u, 0u}, plo[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        float pp[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float pv = ex2(s2[i + u] - m_run[i + u]);
+          l_part[i + u] = l_part[i + u] * alpha[i + u] + pv;
+          pp[u] = pv * ptok;
+        }
+        // P = hi + lo, both e4m3
+        const __nv_fp8x2_storage_t hi2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(pp[0], pp[1]), __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_fp8x2_storage_t lo2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(pp[0] - hf.x, pp[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
+        phi[i >> 2] |= (uint32_t)hi2 << (8 * (i & 3));
+        plo[i >> 2] |= (uint32_t)lo2 << (8 * (i & 3));
+      }
+      {
+        uint8_t* prow = smem + kOffPt + (k & 1) * kPtBytes + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
+        *reinterpret_cast<uint2*>(prow) = make_uint2(phi[0], phi[1]);
+        *reinterpret_cast<uint2*>(prow + kPtSbo) = make_uint2(plo[0], plo[1]);
+      }
+      // ---- P.V of tile k-1 must be complete: O^T rescale below, and the phase of pready ----
+      if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
+      tc_fence_after();
+      if (resc) {
+        const float rs = exp2i(R - Rnew);
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = alpha[i] * rs;
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t a[8], c[8];
+          const uint32_t col = t_lane + kColO + 32 * blk + h0;
+          tmem_ld8_nowait(col, a);
+          tmem_ld8_nowait(col + 16, c);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            a[i] = __float_as_uint(__uint_as_float(a[i]) * f[i]);
+            c[i] = __float_as_uint(__uint_as_float(c[i]) * f[i]);
+          }
+          tmem_st8(col, a);
+          tmem_st8(col + 16, c);
+        }
+        tc_wait_st();
+      }
+      R = Rnew;
+      fence_proxy_async_smem();  // P^T is read by the tensor cores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pready);
+      if (it.last) {
+        // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
+        float* lw = reinterpret_cast<float*>(smem + kOffLw);
+        float* mlast = reinterpret_cast<float*>(smem + kOffMlast);
+        const float ls = warp_reduce8<false>(l_part, lane);
+        if ((lane & 3) == 0) lw[q4 * kHeads + h0 + (lane >> 2)] = ls;
+        if (q4 == 0 && lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mlast[h0 + i] = m_run[i];
+        }
+        named_sync(kBarSm, kSmThreads);
+        const int4 si = p.ws.seqinfo[it.b];
+        const bool whole = si.x == si.y;
+        const int slot = si.z + (g - si.x);
+        float* ofac = reinterpret_cast<float*>(smem + kOffMlast) + kHeads;  // [16] 2^(R-127) / l
+        if (stid < kHeads) {
+          const int h = stid;
+          const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
+          if (!whole) p.ws.part_lse[slot * kHeads + h] = mlast[h] + lg2(L);
+          const float os = (R == 255) ? __int_as_float(0x7FC00000) : exp2i(R - 127);
+          ofac[h] = os / L;
+        }
+        named_sync(kBarSm, kSmThreads);
+        wait_or_flag(bar_pv, k & 1, p, aborted);
+        tc_fence_after();
+#pragma unroll 1
+        for (int sl = 0; sl < 4; ++sl) {
+          const int blk = 2 * part + (sl >> 1);
+          const int hs = 8 * (sl & 1);  // heads hs .. hs+7
+          uint32_t a[8], c[8];
+          const uint32_t col = t_lane + kColO + 32 * blk + hs;
+          tmem_ld8_nowait(col, a);
+          tmem_ld8_nowait(col + 16, c);
+          tc_wait_ld();
+          const int dim = 128 * blk + t;
+          if (whole) {
+            __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[(hs + i) * kDv] = __float2bfloat16_rn((__uint_as_float(a[i]) + __uint_as_float(c[i])) * ofac[hs + i]);
+          } else {
+            float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[(hs + i) * kDv] = (__uint_as_float(a[i]) + __uint_as_float(c[i])) * ofac[hs + i];
+          }
+        }
+        tc_fence_before();
+        named_sync(kBarSm, kSmThreads);  // lw and the accumulator are reused by the next segment
+      }
+      it = nx;
+      ++k;
+    } while (has_next);
+  }
   // every P.V was waited for at its segment's end; the MMA warp has finished issuing
   tc_fence_before();
-  named_sync(2, kTokThreads + 32);
+  named_sync(kBarAll, kTokThreads + 32);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
