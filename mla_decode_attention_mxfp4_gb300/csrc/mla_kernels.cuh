@@ -67,8 +67,14 @@ constexpr int kSmWarps = 8;                  // softmax group: 2 warps per lane 
 constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kTokWarps = kDqWarps + kSmWarps;
 constexpr int kTokThreads = kTokWarps * 32;
-constexpr int kProdWarp = kTokWarps;         // bulk async copies
-constexpr int kMmaWarp = kTokWarps + 1;      // tcgen05.mma issue
+// Warp roles, in warp-index order (lower indices are favoured by the issue
+// schedulers, so the latency-critical roles come first): MMA issue, producer,
+// softmax group, dequant group.  A warp reaches tensor-memory lanes
+// 32*(warp % 4)..+31; both groups cover every quarter.
+constexpr int kMmaWarp = 0;                  // tcgen05.mma issue (also allocates tensor memory)
+constexpr int kProdWarp = 1;                 // bulk async copies
+constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..9
+constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 10..25
 constexpr int kThreads = (kTokWarps + 2) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 
@@ -478,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   if (!any) return;  // cannot happen for g < geff
   bool aborted = false;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
-  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -562,7 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       has_next = nxt.next();
       ++k;
     }
-    named_sync(kBarAll, kTokThreads + 32);  // all issue done before the dealloc
+    // every P.V completed (the softmax group waited for each segment's last one) and
+    // the other groups are done with tensor memory: release it (the allocating warp)
+    named_sync(kBarAll, kTokThreads + 32);
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
     return;
   }
 
@@ -571,16 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
   int* st_buf = reinterpret_cast<int*>(smem + kOffSt);  // [2][128]
 
-  if (warp < kDqWarps) {
+  if (warp >= kDqWarp0) {
     // ======================= dequant group (warps 0..15) ========================
     // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
     // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod 4).
-    const int part = warp >> 2;
-    const int gtid = tid;  // 0..511
+    const int dwarp = warp - kDqWarp0;  // 0..15
+    const int part = dwarp >> 2;
+    const int gtid = tid - kDqWarp0 * 32;  // 0..511
     uint8_t* vt = smem + kOffVt;
     // prologue: tile 0 (a segment start)
     wait_or_flag(&bar_full[0], 0, p, aborted);
-    build_qhat(smem, p.sm_scale, it.seg & 3, gtid, warp, lane);
+    build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
     if (gtid == 0) mbar_arrive(bar_qempty);
     int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA);
     tc_wait_st();
@@ -606,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         if (nx.first) {
           // the next segment's Qhat replaces this one once QK^T of tile k has completed
           wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
-          build_qhat(smem, p.sm_scale, nx.seg & 3, gtid, warp, lane);
+          build_qhat(smem, p.sm_scale, nx.seg & 3, gtid, dwarp, lane);
           if (gtid == 0) mbar_arrive(bar_qempty);
         }
         tc_fence_after();
@@ -659,9 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     // ======================= softmax group (warps 16..23) =======================
     // Warp (q4, part) owns tokens 32*q4.. and heads 8*part..8*part+7 (their running
     // statistics and O^T columns), and O^T blocks 2*part, 2*part+1 at a segment end.
-    const int part = (warp - kDqWarps) >> 2;
+    const int part = (warp - kSmWarp0) >> 2;
     const int h0 = 8 * part;
-    const int stid = tid - kDqThreads;  // 0..255
+    const int stid = tid - kSmWarp0 * 32;  // 0..255
     const float* chs = reinterpret_cast<const float*>(smem + kOffCh);
     float l_part[8], m_run[8];
     int R = 0;
@@ -843,13 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       ++k;
     } while (has_next);
   }
-  // every P.V was waited for at its segment's end; the MMA warp has finished issuing
+  // tensor memory is released by the MMA warp once every group is past this point
   tc_fence_before();
   named_sync(kBarAll, kTokThreads + 32);
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
 }
 
 // ---- merge of split sequences -------------------------------------------------------
