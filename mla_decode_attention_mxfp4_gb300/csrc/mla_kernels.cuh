@@ -61,9 +61,10 @@ constexpr int kPacked = 288;   // bytes per token
 constexpr int kNScale = 18;    // scale bytes per token
 constexpr int kTile = 128;     // tokens per tile
 constexpr int kStages = 3;
-constexpr int kDqWarps = 16;                 // dequant group: 4 warps per tensor-memory lane quarter
+constexpr int kDqWarps = 12;                 // dequant group: 3 warps per tensor-memory lane quarter
 constexpr int kDqThreads = kDqWarps * 32;
-constexpr int kSmWarps = 8;                  // softmax group: 2 warps per lane quarter
+constexpr int kDqParts = kDqWarps / 4;      // dequant warps per lane quarter
+constexpr int kSmWarps = 4;                  // softmax group: 1 warp per lane quarter
 constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kTokWarps = kDqWarps + kSmWarps;
 constexpr int kTokThreads = kTokWarps * 32;
@@ -73,8 +74,8 @@ constexpr int kTokThreads = kTokWarps * 32;
 // 32*(warp % 4)..+31; both groups cover every quarter.
 constexpr int kMmaWarp = 0;                  // tcgen05.mma issue (also allocates tensor memory)
 constexpr int kProdWarp = 1;                 // bulk async copies
-constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..9
-constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 10..25
+constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..5
+constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 6..17
 constexpr int kThreads = (kTokWarps + 2) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 
@@ -122,17 +123,18 @@ constexpr int kOffQStage = kOffStages + kStages * kStageBytes;            // 117
 constexpr int kOffQhat = kOffQStage + kQBytes;                            // 136320
 constexpr int kOffVt = kOffQhat + 32 * kDqk;                              // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
-constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][4][16] tile maxima
+constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][16 heads][4 quarters]
 constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: [2][4] token-exponent maxima
 constexpr int kOffCh = kOffRw + 32;                                       // 229024: [4][16] score factors
 constexpr int kOffEh = kOffCh + 4 * kHeads * 4;                           // 229280
-constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229344: [4][16]
-constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] m, [16] output factors
-constexpr int kOffSt = kOffMlast + 2 * kHeads * 4;                        // 229728: [2][128] token exponents
-constexpr int kOffTmem = kOffSt + 2 * kTile * 4;                          // 230752
-constexpr int kOffBar = kOffTmem + 16;                                    // 230768
+constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229344: [16 heads][4 quarters]
+constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] output factors
+constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229664: [4 warps][16 m, 16 alpha]
+constexpr int kOffSt = kOffMst + 4 * 2 * kHeads * 4;                      // 230176: [2][128] token exponents
+constexpr int kOffTmem = kOffSt + 2 * kTile * 4;                          // 231200
+constexpr int kOffBar = kOffTmem + 16;                                    // 231216
 constexpr int kNumBars = 16;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 230896
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231344
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
@@ -313,13 +315,15 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
 // Segment start: per-head prescale exponent, score factor, and the e4m3 hi/lo
 // parts of Qhat = q * 2^-E_h (two e4m3 terms hold a bf16 value exactly unless it
 // lies more than 2^11 below its head's maximum).  Run by the dequant group
-// (gtid 0..511, one head per warp); ends with the group's barrier.
+// (gtid 0..383; warp w takes heads w and w + 12); ends with the group's barrier.
 __device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int chbuf, int gtid, int gwarp, int lane) {
   const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
   int* eh = reinterpret_cast<int*>(smem + kOffEh);
   float* ch = reinterpret_cast<float*>(smem + kOffCh) + chbuf * kHeads;
-  {
-    const int h = gwarp;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = gwarp + kDqWarps * hh;
+    if (h >= kHeads) break;
     const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
     uint32_t mx = 0;
 #pragma unroll 6
@@ -362,9 +366,28 @@ __device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int ch
   named_sync(kBarDq, kDqThreads);
 }
 
+// f16 2^r as the bit pattern of an f16x2 pair: exponent field r + 15 when normal, a
+// subnormal bit down to 2^-24, else 0 (r <= 0).
+__device__ __forceinline__ uint32_t f16x2_pow2(int r) {
+  const uint32_t hb = r >= -14 ? (uint32_t)(r + 15) << 10 : (r >= -24 ? 1u << (r + 24) : 0u);
+  return hb * 0x10001u;
+}
+// 32 e2m1 codes (one 16-byte chunk) times an f16x2 factor -> 32 e5m2 bytes.
+__device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32_t (&e)[8]) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t v[4];
+    e2m1x8_to_f16x8(ws[i], v);
+    e[2 * i] = f16x4_hi_bytes(hmul2_u32(v[0], f2), hmul2_u32(v[1], f2));
+    e[2 * i + 1] = f16x4_hi_bytes(hmul2_u32(v[2], f2), hmul2_u32(v[3], f2));
+  }
+}
+
 // K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
 // s_tb >= S_t - 15 (the truncated high byte of an f16 with <= 2 significant bits).
-// Token t = this thread's lane of the quarter; blocks b == part (mod 4).
+// Token t = this thread's lane of the quarter; blocks b == part (mod 3), software
+// pipelined (the next block's bytes are loaded while this one is converted).
 // Returns S_t (0 for tokens past the tile).
 __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane) {
   const bool valid = t < n;
@@ -382,62 +405,59 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
     }
     St = (int)max(mhi >> 8, mlo);
   }
-  const uint8_t* row = st + t * kPacked;
-#pragma unroll 2
-  for (int j = 0; j < 5; ++j) {
-    const int b = part + 4 * j;
-    if (b < kNScale) {
-      const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * b);
-      // f16 2^(s - S_t): exponent field s - S_t + 15 when normal, a subnormal bit down to 2^-24, else 0
-      uint32_t hb = 0;
-      if (valid) {
-        const int r = (int)sb[b] - St;
-        hb = r >= -14 ? (uint32_t)(r + 15) << 10 : (r >= -24 ? 1u << (r + 24) : 0u);
-      }
-      const uint32_t f2 = hb * 0x10001u;
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-      uint32_t e[8];
+  const uint8_t* row = st + t * kPacked + 16 * part;
+  const uint8_t* sbp = sb + part;
+  constexpr int kNb = kNScale / kDqParts;  // 6 blocks per part
+  uint4 wn = *reinterpret_cast<const uint4*>(row);
+  int sn = valid ? (int)sbp[0] : 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t v[4];
-        e2m1x8_to_f16x8(ws[i], v);
-        e[2 * i] = f16x4_hi_bytes(hmul2_u32(v[0], f2), hmul2_u32(v[1], f2));
-        e[2 * i + 1] = f16x4_hi_bytes(hmul2_u32(v[2], f2), hmul2_u32(v[3], f2));
-      }
-      tmem_st8(a_lane + 8 * b, e);
+  for (int j = 0; j < kNb; ++j) {
+    const uint4 w = wn;
+    const int s = sn;
+    if (j + 1 < kNb) {
+      wn = *reinterpret_cast<const uint4*>(row + 16 * kDqParts * (j + 1));
+      sn = valid ? (int)sbp[kDqParts * (j + 1)] : 0;
     }
+    const uint32_t f2 = valid ? f16x2_pow2(s - St) : 0u;
+    uint32_t e[8];
+    chunk_to_e5m2(w, f2, e);
+    tmem_st8(a_lane + 8 * (part + kDqParts * j), e);
   }
   return St;
 }
 
-// Maximum (kMax) or sum over the 32 lanes of eight per-lane values; lane L ends
-// with the result for value index 4*b4 + 2*b3 + b2 (b_i = bit i of L).
+// Maximum (kMax) or sum over the 32 lanes of sixteen per-lane values; lane L ends
+// with the result for value index L >> 1.
 template <bool kMax>
-__device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane) {
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-  float a[4], c[2];
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+  float a[8], c[4], d[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b4 ? v[i] : v[i + 4], keep = b4 ? v[i + 4] : v[i];
+  for (int i = 0; i < 8; ++i) {  // lanes with bit 4 keep values 8..15
+    const float send = b4 ? v[i] : v[i + 8], keep = b4 ? v[i + 8] : v[i];
     const float r = __shfl_xor_sync(0xffffffffu, send, 16);
     a[i] = kMax ? fmaxf(keep, r) : keep + r;
   }
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b3 ? a[i] : a[i + 2], keep = b3 ? a[i + 2] : a[i];
+  for (int i = 0; i < 4; ++i) {
+    const float send = b3 ? a[i] : a[i + 4], keep = b3 ? a[i + 4] : a[i];
     const float r = __shfl_xor_sync(0xffffffffu, send, 8);
     c[i] = kMax ? fmaxf(keep, r) : keep + r;
   }
-  float d;
-  {
-    const float send = b2 ? c[0] : c[1], keep = b2 ? c[1] : c[0];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b2 ? c[i] : c[i + 2], keep = b2 ? c[i + 2] : c[i];
     const float r = __shfl_xor_sync(0xffffffffu, send, 4);
-    d = kMax ? fmaxf(keep, r) : keep + r;
+    d[i] = kMax ? fmaxf(keep, r) : keep + r;
   }
-  const float r2 = __shfl_xor_sync(0xffffffffu, d, 2);
-  d = kMax ? fmaxf(d, r2) : d + r2;
-  const float r1 = __shfl_xor_sync(0xffffffffu, d, 1);
-  return kMax ? fmaxf(d, r1) : d + r1;
+  float x;
+  {
+    const float send = b1 ? d[0] : d[1], keep = b1 ? d[1] : d[0];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 2);
+    x = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  const float r1 = __shfl_xor_sync(0xffffffffu, x, 1);
+  return kMax ? fmaxf(x, r1) : x + r1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
@@ -582,12 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   int* st_buf = reinterpret_cast<int*>(smem + kOffSt);  // [2][128]
 
   if (warp >= kDqWarp0) {
-    // ======================= dequant group (warps 0..15) ========================
+    // ======================= dequant group (warps 6..17) ========================
     // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
-    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod 4).
-    const int dwarp = warp - kDqWarp0;  // 0..15
+    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod 3).
+    const int dwarp = warp - kDqWarp0;  // 0..7
     const int part = dwarp >> 2;
-    const int gtid = tid - kDqWarp0 * 32;  // 0..511
+    const int gtid = tid - kDqWarp0 * 32;  // 0..383
     uint8_t* vt = smem + kOffVt;
     // prologue: tile 0 (a segment start)
     wait_or_flag(&bar_full[0], 0, p, aborted);
@@ -637,15 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       {
         const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
         uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
+        // V blocks b == part (mod 3), b < 16: 6, 5, 5 of them
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-          uint32_t e[2][8];
+          uint32_t e[3][8];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) tmem_ld8_nowait(acol + 8 * (part + 4 * (2 * hb + j)), e[j]);
+          for (int j = 0; j < 3; ++j) {
+            const int b = part + kDqParts * (3 * hb + j);
+            if (b < kDv / 32) tmem_ld8_nowait(acol + 8 * b, e[j]);
+          }
           tc_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int b = part + 4 * (2 * hb + j);  // dims 32b .. 32b+31
+          for (int j = 0; j < 3; ++j) {
+            const int b = part + kDqParts * (3 * hb + j);  // dims 32b .. 32b+31
+            if (b >= kDv / 32) continue;
             uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
             *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
             *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
@@ -667,14 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       ++k;
     } while (has_next);
   } else {
-    // ======================= softmax group (warps 16..23) =======================
-    // Warp (q4, part) owns tokens 32*q4.. and heads 8*part..8*part+7 (their running
-    // statistics and O^T columns), and O^T blocks 2*part, 2*part+1 at a segment end.
-    const int part = (warp - kSmWarp0) >> 2;
-    const int h0 = 8 * part;
-    const int stid = tid - kSmWarp0 * 32;  // 0..255
+    // ======================= softmax group (warps 2..5) =========================
+    // Warp q4 owns tokens 32*q4.. of each tile and all 16 heads; lane L keeps the
+    // running statistics of head L >> 1 (in shared memory, shared by the lane pair).
+    const int sw = warp - kSmWarp0;  // 0..3
+    const int stid = tid - kSmWarp0 * 32;  // 0..127
     const float* chs = reinterpret_cast<const float*>(smem + kOffCh);
-    float l_part[8], m_run[8];
+    float* mstate = reinterpret_cast<float*>(smem + kOffMst) + sw * 2 * kHeads;  // [16] m, [16] alpha*resc
+    float l_part[16];
     int R = 0;
     int k = 0;
     bool has_next;
@@ -689,71 +714,75 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       const float stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
       wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
       tc_fence_after();
-      float s2[8];
-      float* hmax = reinterpret_cast<float*>(smem + kOffHmax) + (k & 1) * 4 * kHeads;
+      float s2[16];
+      float* hmax = reinterpret_cast<float*>(smem + kOffHmax) + (k & 1) * 4 * kHeads;  // [16 heads][4 quarters]
       int* rwb = reinterpret_cast<int*>(smem + kOffRw) + (k & 1) * 4;
       {
-        uint32_t rh[8], rl[8];
-        const uint32_t scol = t_lane + kColS + 32 * (k & 1) + h0;
-        tmem_ld8_nowait(scol, rh);
-        tmem_ld8_nowait(scol + 16, rl);
+        uint32_t rh[16], rl[16];
+        const uint32_t scol = t_lane + kColS + 32 * (k & 1);
+        tmem_ld16_nowait(scol, rh);
+        tmem_ld16_nowait(scol + 16, rl);
         tc_wait_ld();
-        const float cs = stok;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          s2[i] = valid ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * (ch[h0 + i] * cs) : -INFINITY;
-        const float wm = warp_reduce8<true>(s2, lane);
-        if ((lane & 3) == 0) hmax[q4 * kHeads + h0 + (lane >> 2)] = wm;
+        for (int i = 0; i < 16; i += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(ch + i);
+          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            s2[i + u] = valid ? (__uint_as_float(rh[i + u]) + __uint_as_float(rl[i + u])) * (cc[u] * stok) : -INFINITY;
+        }
+        const float wm = warp_reduce16<true>(s2, lane);
+        if ((lane & 1) == 0) hmax[(lane >> 1) * 4 + q4] = wm;
       }
       const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
-      if (lane == 0 && part == 0) rwb[q4] = rw;
+      if (lane == 0) rwb[q4] = rw;
       named_sync(kBarSm, kSmThreads);
-      // running statistics of this warp's heads (every lane computes the same values)
-      float alpha[8];
+      // running statistics: lane L computes head L >> 1; the lane pair agrees
       int Rnew;
       bool resc;
       {
         const int4 rwv = *reinterpret_cast<const int4*>(rwb);
         const int Rtile = max(max(rwv.x, rwv.y), max(rwv.z, rwv.w));
         Rnew = seg_first ? Rtile : (Rtile > R + kMaxThresh ? Rtile : R);
-        resc = !seg_first && Rnew != R;
-#pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          float M[4];
-          const float4 a0 = *reinterpret_cast<const float4*>(hmax + h0 + 4 * hv);
-          const float4 a1 = *reinterpret_cast<const float4*>(hmax + kHeads + h0 + 4 * hv);
-          const float4 a2 = *reinterpret_cast<const float4*>(hmax + 2 * kHeads + h0 + 4 * hv);
-          const float4 a3 = *reinterpret_cast<const float4*>(hmax + 3 * kHeads + h0 + 4 * hv);
-          M[0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-          M[1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-          M[2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-          M[3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = 4 * hv + u;
-            if (seg_first) {
-              m_run[i] = M[u];
-              alpha[i] = 0.f;
-              l_part[i] = 0.f;
-            } else if (M[u] > m_run[i] + (float)kMaxThresh) {
-              alpha[i] = ex2(m_run[i] - M[u]);
-              m_run[i] = M[u];
-              resc = true;
-            } else {
-              alpha[i] = 1.f;
-            }
-          }
+        const int h = lane >> 1;
+        const float4 hm = *reinterpret_cast<const float4*>(hmax + h * 4);
+        const float M = fmaxf(fmaxf(hm.x, hm.y), fmaxf(hm.z, hm.w));
+        const float mo = mstate[h];
+        float mn = mo, alpha = 1.f;
+        bool moved = false;
+        if (seg_first) {
+          mn = M;
+          alpha = 0.f;
+        } else if (M > mo + (float)kMaxThresh) {
+          mn = M;
+          alpha = ex2(mo - M);
+          moved = true;
         }
+        resc = __any_sync(0xffffffffu, moved) || (!seg_first && Rnew != R);
+        __syncwarp();
+        if ((lane & 1) == 0) {
+          mstate[h] = mn;
+          mstate[kHeads + h] = alpha;
+        }
+        __syncwarp();
+      }
+      float m_now[16], alpha_v[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(mstate + i);
+        const float4 b = *reinterpret_cast<const float4*>(mstate + kHeads + i);
+        m_now[i] = a.x; m_now[i + 1] = a.y; m_now[i + 2] = a.z; m_now[i + 3] = a.w;
+        alpha_v[i] = b.x; alpha_v[i + 1] = b.y; alpha_v[i + 2] = b.z; alpha_v[i + 3] = b.w;
       }
       const float ptok = valid ? exp2i(St - Rnew) : 0.f;
-      uint32_t phi[2] = {0u, 0u}, plo[2] = {0u, 0u};
+      uint32_t phi[4], plo[4];
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
+      for (int i = 0; i < 16; i += 2) {
         float pp[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float pv = ex2(s2[i + u] - m_run[i + u]);
-          l_part[i + u] = l_part[i + u] * alpha[i + u] + pv;
+          const float pv = ex2(s2[i + u] - m_now[i + u]);
+          l_part[i + u] = seg_first ? pv : l_part[i + u] * alpha_v[i + u] + pv;
           pp[u] = pv * ptok;
         }
         // P = hi + lo, both e4m3
@@ -763,36 +792,39 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
         const __nv_fp8x2_storage_t lo2 =
             __nv_cvt_float2_to_fp8x2(make_float2(pp[0] - hf.x, pp[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
-        phi[i >> 2] |= (uint32_t)hi2 << (8 * (i & 3));
-        plo[i >> 2] |= (uint32_t)lo2 << (8 * (i & 3));
+        if ((i & 2) == 0) {
+          phi[i >> 2] = (uint32_t)hi2;
+          plo[i >> 2] = (uint32_t)lo2;
+        } else {
+          phi[i >> 2] |= (uint32_t)hi2 << 16;
+          plo[i >> 2] |= (uint32_t)lo2 << 16;
+        }
       }
       {
-        uint8_t* prow = smem + kOffPt + (k & 1) * kPtBytes + (t >> 3) * kPtLbo + (t & 7) * 16 + h0;
-        *reinterpret_cast<uint2*>(prow) = make_uint2(phi[0], phi[1]);
-        *reinterpret_cast<uint2*>(prow + kPtSbo) = make_uint2(plo[0], plo[1]);
+        uint8_t* prow = smem + kOffPt + (k & 1) * kPtBytes + (t >> 3) * kPtLbo + (t & 7) * 16;
+        *reinterpret_cast<uint4*>(prow) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
+        *reinterpret_cast<uint4*>(prow + kPtSbo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
       }
       // ---- P.V of tile k-1 must be complete: O^T rescale below, and the phase of pready ----
       if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
       tc_fence_after();
       if (resc) {
         const float rs = exp2i(R - Rnew);
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = alpha[i] * rs;
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
-          uint32_t a[8], c[8];
-          const uint32_t col = t_lane + kColO + 32 * blk + h0;
-          tmem_ld8_nowait(col, a);
-          tmem_ld8_nowait(col + 16, c);
+          uint32_t a[16], c[16];
+          const uint32_t col = t_lane + kColO + 32 * blk;
+          tmem_ld16_nowait(col, a);
+          tmem_ld16_nowait(col + 16, c);
           tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            a[i] = __float_as_uint(__uint_as_float(a[i]) * f[i]);
-            c[i] = __float_as_uint(__uint_as_float(c[i]) * f[i]);
+          for (int i = 0; i < 16; ++i) {
+            const float f = alpha_v[i] * rs;
+            a[i] = __float_as_uint(__uint_as_float(a[i]) * f);
+            c[i] = __float_as_uint(__uint_as_float(c[i]) * f);
           }
-          tmem_st8(col, a);
-          tmem_st8(col + 16, c);
+          tmem_st16(col, a);
+          tmem_st16(col + 16, c);
         }
         tc_wait_st();
       }
@@ -803,52 +835,52 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       if (lane == 0) mbar_arrive(bar_pready);
       if (it.last) {
         // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
-        float* lw = reinterpret_cast<float*>(smem + kOffLw);
-        float* mlast = reinterpret_cast<float*>(smem + kOffMlast);
-        const float ls = warp_reduce8<false>(l_part, lane);
-        if ((lane & 3) == 0) lw[q4 * kHeads + h0 + (lane >> 2)] = ls;
-        if (q4 == 0 && lane == 0) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mlast[h0 + i] = m_run[i];
-        }
+        float* lw = reinterpret_cast<float*>(smem + kOffLw);      // [16 heads][4 quarters]
+        float* ofac = reinterpret_cast<float*>(smem + kOffMlast);  // [16] 2^(R-127) / l
+        const float ls = warp_reduce16<false>(l_part, lane);
+        if ((lane & 1) == 0) lw[(lane >> 1) * 4 + q4] = ls;
         named_sync(kBarSm, kSmThreads);
         const int4 si = p.ws.seqinfo[it.b];
         const bool whole = si.x == si.y;
         const int slot = si.z + (g - si.x);
-        float* ofac = reinterpret_cast<float*>(smem + kOffMlast) + kHeads;  // [16] 2^(R-127) / l
         if (stid < kHeads) {
           const int h = stid;
-          const float L = lw[h] + lw[kHeads + h] + lw[2 * kHeads + h] + lw[3 * kHeads + h];
-          if (!whole) p.ws.part_lse[slot * kHeads + h] = mlast[h] + lg2(L);
+          const float4 l4 = *reinterpret_cast<const float4*>(lw + h * 4);
+          const float L = (l4.x + l4.y) + (l4.z + l4.w);
+          if (!whole) p.ws.part_lse[slot * kHeads + h] = mstate[h] + lg2(L);
           const float os = (R == 255) ? __int_as_float(0x7FC00000) : exp2i(R - 127);
           ofac[h] = os / L;
         }
         named_sync(kBarSm, kSmThreads);
         wait_or_flag(bar_pv, k & 1, p, aborted);
         tc_fence_after();
+        float of[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 f4 = *reinterpret_cast<const float4*>(ofac + i);
+          of[i] = f4.x; of[i + 1] = f4.y; of[i + 2] = f4.z; of[i + 3] = f4.w;
+        }
 #pragma unroll 1
-        for (int sl = 0; sl < 4; ++sl) {
-          const int blk = 2 * part + (sl >> 1);
-          const int hs = 8 * (sl & 1);  // heads hs .. hs+7
-          uint32_t a[8], c[8];
-          const uint32_t col = t_lane + kColO + 32 * blk + hs;
-          tmem_ld8_nowait(col, a);
-          tmem_ld8_nowait(col + 16, c);
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t a[16], c[16];
+          const uint32_t col = t_lane + kColO + 32 * blk;
+          tmem_ld16_nowait(col, a);
+          tmem_ld16_nowait(col + 16, c);
           tc_wait_ld();
           const int dim = 128 * blk + t;
           if (whole) {
             __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[(hs + i) * kDv] = __float2bfloat16_rn((__uint_as_float(a[i]) + __uint_as_float(c[i])) * ofac[hs + i]);
+            for (int h = 0; h < kHeads; ++h)
+              o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h]);
           } else {
             float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[(hs + i) * kDv] = (__uint_as_float(a[i]) + __uint_as_float(c[i])) * ofac[hs + i];
+            for (int h = 0; h < kHeads; ++h) o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h];
           }
         }
         tc_fence_before();
-        named_sync(kBarSm, kSmThreads);  // lw and the accumulator are reused by the next segment
+        named_sync(kBarSm, kSmThreads);  // lw, ofac and the accumulator are reused by the next segment
       }
       it = nx;
       ++k;
