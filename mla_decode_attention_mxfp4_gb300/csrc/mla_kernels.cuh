@@ -386,7 +386,7 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
 
 // K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
 // s_tb >= S_t - 15 (the truncated high byte of an f16 with <= 2 significant bits).
-// Token t = this thread's lane of the quarter; blocks b == part (mod 3), software
+// Token t = this thread's lane of the quarter; blocks b == part (mod kDqParts), software
 // pipelined (the next block's bytes are loaded while this one is converted).
 // Returns S_t (0 for tokens past the tile).
 __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane) {
@@ -407,14 +407,15 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
   }
   const uint8_t* row = st + t * kPacked + 16 * part;
   const uint8_t* sbp = sb + part;
-  constexpr int kNb = kNScale / kDqParts;  // 6 blocks per part
+  constexpr int kNb = (kNScale + kDqParts - 1) / kDqParts;  // blocks per part (the last ones may be absent)
   uint4 wn = *reinterpret_cast<const uint4*>(row);
   int sn = valid ? (int)sbp[0] : 0;
 #pragma unroll
   for (int j = 0; j < kNb; ++j) {
+    if (part + kDqParts * j >= kNScale) break;
     const uint4 w = wn;
     const int s = sn;
-    if (j + 1 < kNb) {
+    if (j + 1 < kNb && part + kDqParts * (j + 1) < kNScale) {
       wn = *reinterpret_cast<const uint4*>(row + 16 * kDqParts * (j + 1));
       sn = valid ? (int)sbp[kDqParts * (j + 1)] : 0;
     }
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   if (warp >= kDqWarp0) {
     // ======================= dequant group (warps 6..17) ========================
     // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
-    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod 3).
+    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod kDqParts).
     const int dwarp = warp - kDqWarp0;  // 0..7
     const int part = dwarp >> 2;
     const int gtid = tid - kDqWarp0 * 32;  // 0..383
@@ -657,19 +658,21 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       {
         const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
         uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
-        // V blocks b == part (mod 3), b < 16: 6, 5, 5 of them
+        // V blocks b == part (mod kDqParts), b < 16, in batches of three
+        constexpr int kNv = (kDv / 32 + kDqParts - 1) / kDqParts;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
+        for (int hb = 0; hb < (kNv + 2) / 3; ++hb) {
           uint32_t e[3][8];
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int b = part + kDqParts * (3 * hb + j);
-            if (b < kDv / 32) tmem_ld8_nowait(acol + 8 * b, e[j]);
+            if (3 * hb + j < kNv && b < kDv / 32) tmem_ld8_nowait(acol + 8 * b, e[j]);
           }
           tc_wait_ld();
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int b = part + kDqParts * (3 * hb + j);  // dims 32b .. 32b+31
+            if (3 * hb + j >= kNv) continue;
             if (b >= kDv / 32) continue;
             uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
             *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
