@@ -123,7 +123,7 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
   mla::mla_split_kernel<<<di.grid, mla::kThreads, mla::kSmemBytes, stream>>>(sp);
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  mla::mla_merge_kernel<<<batch, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(out), w, batch);
+  mla::mla_merge_kernel<<<batch, mla::kMergeThreads, 0, stream>>>(static_cast<__nv_bfloat16*>(out), w, batch);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -78,6 +78,7 @@ constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..5
 constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 6..17
 constexpr int kThreads = (kTokWarps + 2) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
+constexpr int kPartSmemSeqs = 8192;  // the partition kernel keeps ipc in shared memory up to this batch
 
 constexpr int kDeviceBadIndptr = 1;
 constexpr int kDeviceTimeout = 2;
@@ -238,7 +239,9 @@ __global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __re
                                                              int G, int kv_null, Workspace ws) {
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
+  __shared__ int s_ipc[kPartSmemSeqs + 1];  // copy of ipc for batch <= kPartSmemSeqs
   const int tid = threadIdx.x;
+  const bool in_smem = B <= kPartSmemSeqs;
   if (tid == 0) s_bad = 0;
   __syncthreads();
   const int hi = kv_null ? 0 : max(indptr[B], 0);
@@ -251,13 +254,17 @@ __global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __re
     int tot;
     int pm = block_inclusive_scan<true>(v, warp_tot, tot);
     pm = max(pm, carry);
-    if (i <= B) ws.ipc[i] = min(max(pm, 0), hi);
+    if (i <= B) {
+      const int c = min(max(pm, 0), hi);
+      ws.ipc[i] = c;
+      if (in_smem) s_ipc[i] = c;
+    }
     carry = max(carry, tot);
     __syncthreads();
   }
   __threadfence_block();
   __syncthreads();
-  const int* ipc = ws.ipc;
+  const int* ipc = in_smem ? s_ipc : ws.ipc;
   const int rbase = ipc[0];
   const int N = ipc[B] - rbase;
   const long long per_ll = max((long long)kMinPerCta, ((long long)N + G - 1) / G);
@@ -895,57 +902,83 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 }
 
 // ---- merge of split sequences -------------------------------------------------------
-__global__ void __launch_bounds__(256) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws, int B) {
+// One CTA per sequence, warp h = head h, lane l = dims 16l..16l+15:
+// out = sum_s 2^(lse_s - M) acc_s / sum_s 2^(lse_s - M), M = max_s lse_s; empty -> zeros.
+constexpr int kMergeThreads = 32 * kHeads;
+__global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws,
+                                                                  int B) {
   const int b = blockIdx.x;
   if (b >= B) return;
-  const int4 si = ws.seqinfo[b];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
   const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1];
+  uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
   if (a1 <= a0) {  // empty sequence -> zeros
-    uint4* o = reinterpret_cast<uint4*>(out + (long long)b * kHeads * kDv);
-    for (int i = tid; i < kHeads * kDv / 8; i += 256) o[i] = make_uint4(0, 0, 0, 0);
+    dst[0] = make_uint4(0, 0, 0, 0);
+    dst[1] = make_uint4(0, 0, 0, 0);
     return;
   }
+  const int4 si = ws.seqinfo[b];
   const int ns = si.y - si.x + 1;
   if (ns < 2) return;  // written by the split kernel
   const int base = si.z;
+  // lane i holds the weight of partials i, i+32, ...; M over all partials first
+  float M = -INFINITY;
+  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ws.part_lse[(base + i) * kHeads + h]);
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = warp * 2 + hh;
-    float M = -INFINITY;
-    for (int i = lane; i < ns; i += 32) M = fmaxf(M, ws.part_lse[(base + i) * kHeads + h]);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[16];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int i = lane; i < ns; i += 32) L += ex2(ws.part_lse[(base + i) * kHeads + h] - M);
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  float L = 0.f;
+  for (int c0 = 0; c0 < ns; c0 += 32) {
+    const int cn = min(32, ns - c0);
+    const float wl = lane < cn ? ex2(ws.part_lse[(base + c0 + lane) * kHeads + h] - M) : 0.f;
+    L += wl;
+    int i = 0;
+    for (; i + 1 < cn; i += 2) {  // two partials' loads in flight
+      const float w0 = __shfl_sync(0xffffffffu, wl, i), w1 = __shfl_sync(0xffffffffu, wl, i + 1);
+      const float4* s0 =
+          reinterpret_cast<const float4*>(ws.part_acc + ((long long)(base + c0 + i) * kHeads + h) * kDv + lane * 16);
+      const float4* s1 = s0 + kHeads * kDv / 4;
+      float4 x0[4], x1[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    float accv[16];
+      for (int q = 0; q < 4; ++q) {
+        x0[q] = s0[q];
+        x1[q] = s1[q];
+      }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) accv[i] = 0.f;
-    for (int i = 0; i < ns; ++i) {
-      const float w = ex2(ws.part_lse[(base + i) * kHeads + h] - M);
-      const float4* src = reinterpret_cast<const float4*>(ws.part_acc + ((long long)(base + i) * kHeads + h) * kDv + lane * 16);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 x = src[q4];
-        accv[4 * q4] += w * x.x;
-        accv[4 * q4 + 1] += w * x.y;
-        accv[4 * q4 + 2] += w * x.z;
-        accv[4 * q4 + 3] += w * x.w;
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q] += w0 * x0[q].x + w1 * x1[q].x;
+        acc[4 * q + 1] += w0 * x0[q].y + w1 * x1[q].y;
+        acc[4 * q + 2] += w0 * x0[q].z + w1 * x1[q].z;
+        acc[4 * q + 3] += w0 * x0[q].w + w1 * x1[q].w;
       }
     }
-    const float inv = 1.f / L;
-    uint32_t pk[8];
+    if (i < cn) {
+      const float w0 = __shfl_sync(0xffffffffu, wl, i);
+      const float4* s0 =
+          reinterpret_cast<const float4*>(ws.part_acc + ((long long)(base + c0 + i) * kHeads + h) * kDv + lane * 16);
 #pragma unroll
-    for (int q2 = 0; q2 < 8; ++q2) {
-      __nv_bfloat162 bv = __floats2bfloat162_rn(accv[2 * q2] * inv, accv[2 * q2 + 1] * inv);
-      pk[q2] = *reinterpret_cast<uint32_t*>(&bv);
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = s0[q];
+        acc[4 * q] += w0 * x.x;
+        acc[4 * q + 1] += w0 * x.y;
+        acc[4 * q + 2] += w0 * x.z;
+        acc[4 * q + 3] += w0 * x.w;
+      }
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
-    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = 1.f / L;
+  uint32_t pk[8];
+#pragma unroll
+  for (int q2 = 0; q2 < 8; ++q2) {
+    __nv_bfloat162 bv = __floats2bfloat162_rn(acc[2 * q2] * inv, acc[2 * q2 + 1] * inv);
+    pk[q2] = *reinterpret_cast<uint32_t*>(&bv);
+  }
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
 }  // namespace mla
