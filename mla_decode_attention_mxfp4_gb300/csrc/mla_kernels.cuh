@@ -417,7 +417,8 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
   constexpr int kNb = (kNScale + kDqParts - 1) / kDqParts;  // blocks per part (the last ones may be absent)
   uint4 wn = *reinterpret_cast<const uint4*>(row);
   int sn = valid ? (int)sbp[0] : 0;
-#pragma unroll
+  // unrolled by two only: the warp roles of a CTA share the instruction caches
+#pragma unroll 2
   for (int j = 0; j < kNb; ++j) {
     if (part + kDqParts * j >= kNScale) break;
     const uint4 w = wn;
