@@ -13,36 +13,38 @@
 //     token stream [indptr[0], indptr[B]) into G equal contiguous ranges (one per
 //     resident CTA), and records, per sequence, which ranges it touches and where
 //     its partial results go.
-//  2. mla_split_kernel (G persistent CTAs): each CTA walks its range in tiles of
-//     128 tokens, one segment per sequence it overlaps.
-//       warp 16     producer: bulk async copies (packed rows, scale bytes, and the
-//                   query rows at a segment start) into a 3-stage smem ring.
-//       warps 0..15 token warps: warp w serves tokens 32(w%4)..+31 (its tensor-
-//                   memory lane quarter) and part w/4 of each token's work:
-//                   - E8M0 exponents -> per-token rebased fp16 factors;
-//                   - K tile (fp16, cvt.e2m1x2 + factor) -> tensor memory, and
-//                     S^T = K . Qhat^T on tcgen05 (kind::f16, A from tensor memory);
-//                   - V tile (dims 0..511) read back from tensor memory and
-//                     stored as e4m3 into shared memory (MN-major);
-//                   - online softmax; P split into e4m3 hi + lo parts (stacked as
-//                     N = 32) and O^T += V^T . P^T on tcgen05 (kind::f8f6f4) into a
-//                     tensor-memory accumulator; the P.V of tile k overlaps the
-//                     K-tile work of tile k+1.
+//  2. mla_split_kernel (G persistent CTAs, one per SM): each CTA walks its range in
+//     tiles of 128 tokens, one segment per sequence it overlaps.  Warp roles:
+//       warp 0      MMA issue (one elected lane per tcgen05.mma, whole warp
+//                   converged) and the tensor-memory allocation;
+//       warp 1      producer: bulk async copies (packed rows, scale bytes, and the
+//                   query rows at a segment start) into a 3-stage smem ring;
+//       warps 2..5  softmax group, one warp per tensor-memory lane quarter (32
+//                   tokens), all 16 heads: online softmax of S^T, P as e4m3 hi + lo
+//                   parts, rescaling of the O^T accumulator, segment epilogue;
+//       warps 6..17 dequant group, three warps per lane quarter: per-token scale
+//                   rebasing, the K tile as e5m2 into tensor memory (A operand of
+//                   QK^T, double-buffered), V^T as e5m2 into shared memory, the
+//                   query operand at a segment start.
+//     QK^T (S^T[128 tokens][32] = K . Qhat^T, hi and lo query parts stacked as N)
+//     and P.V (O^T[512][32] += V^T . P^T) run on tcgen05 kind::f8f6f4 with fp32
+//     accumulators in tensor memory.  The groups hand tiles to each other through
+//     mbarriers only, so tile k+1's dequant overlaps tile k's QK^T, softmax and P.V.
 //     A segment that is a whole sequence writes bf16 output directly; otherwise
 //     it writes a normalised fp32 partial and its log2-sum-exp.
-//  3. mla_merge_kernel (one CTA per sequence): merges the partials of split
-//     sequences with weights 2^(lse_s - max lse); empty sequences get zeros.
+//  3. mla_merge_kernel (one CTA per sequence, one warp per head): merges the
+//     partials of split sequences with weights 2^(lse_s - max lse); empty
+//     sequences get zeros.
 //
-// Numerics: K elements are formed exactly in fp16 as e2m1 * 2^(s_tb - S_t), S_t
-// the largest scale exponent of token t (exact unless a token's blocks span more
-// than 2^23); the token factor 2^(S_t - 127) multiplies the fp32 score.  Q is
-// carried in fp16 with a per-head power-of-two prescale.  V uses the same values
-// in e4m3, exact when a token's 16 V-block exponents lie within 8 of S_t (smaller
-// blocks lose precision relative to the token's largest block).  P is rebased
-// against a running maximum that is only raised when the tile maximum exceeds it
-// by more than 2^4 (scores) or 2^4 (token exponents), so P * 2^(S_t - R) <= 256
-// fits e4m3; it is carried as hi + lo e4m3 parts (about 8 significant bits).
-// Scores, softmax statistics, accumulation and the merge are fp32.
+// Numerics: e2m1 * 2^(s_tb - S_t), S_t the largest scale exponent of token t, has at
+// most two significant bits, so it is exact in e5m2 (the high byte of its fp16 form)
+// for s_tb >= S_t - 15; the token factor 2^(S_t - 127) multiplies the fp32 score and
+// is rebased in P.  The query is q * 2^-E_h (E_h per head) as two e4m3 terms, which
+// hold a bf16 value exactly unless it lies more than 2^11 below its head's maximum.
+// P is rebased against a running maximum that is only raised when the tile maximum
+// exceeds it by more than 2^4 (scores) or 2^4 (token exponents), so
+// P * 2^(S_t - R) <= 256 fits e4m3; it is carried as hi + lo e4m3 parts (about 8
+// significant bits).  Scores, softmax statistics, accumulation and the merge are fp32.
 #pragma once
 #include <climits>
 #include <cstdint>
