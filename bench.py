@@ -220,6 +220,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the default process group (the slowest
+    rank's time); the values themselves on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_gbps(world, nbytes_per_rank, ms):
+    """Whole-job GB/s: the bytes every rank processed in one step over the slowest rank's step time."""
+    return world * nbytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -340,10 +357,7 @@ def run_native(args):
     e2e_ms = ea.elapsed_time(eb) / e2e_steps
     barrier()
 
-    if ws > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], dev)
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
@@ -352,7 +366,7 @@ def run_native(args):
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     line = {
         "metric": "MLA decode achieved HBM GB/s (and us/call)",
-        "value": ws * nbytes / (ms * 1e-3) / 1e9,
+        "value": whole_job_gbps(ws, nbytes, ms),
         "unit": "GB/s",
         "us_per_call": ms * 1e3,
         "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
@@ -368,7 +382,7 @@ def run_native(args):
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                      "split_kernel_us": split_ms * 1e3,
                      "traffic": _traffic_per_launch(args.workload)},
-        "e2e": {"value": ws * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "us_per_call": e2e_ms * 1e3,
+        "e2e": {"value": whole_job_gbps(ws, nbytes, e2e_ms), "unit": "GB/s", "us_per_call": e2e_ms * 1e3,
                 "h2d_bytes_per_step": in_bytes + d.kv_indptr.numel() * 4,
                 "d2h_bytes_per_step": d.batch * 16 * 512 * 2},
         "gpu_launches": 3 * args.steps,
