@@ -88,13 +88,19 @@ def device_status(stream: torch.cuda.Stream | None = None, workspace: torch.Tens
 class HostDecoder:
     """End-to-end decode from pinned host buffers: H2D copies, decode, D2H of the output.
 
-    Device buffers are allocated once for the largest shape seen; each call issues
-    one copy per input, the decode kernels, and one copy back, on `stream`.
+    Device buffers are allocated once for the largest shape seen.  The batch is cut into
+    `chunks` groups of whole sequences with about equal KV rows; the copies of group c+1
+    (on a copy stream) overlap the decode of group c (on the compute stream).  kv_indptr
+    holds absolute row indices, so every group decodes against the full device KV buffer
+    through its own slice of the indptr, with no rebasing.  A kv_indptr that is not a
+    non-decreasing sequence within the rows is sent as one group.
     """
 
-    def __init__(self, device="cuda"):
+    def __init__(self, device="cuda", chunks: int = 4):
         self.device = torch.device(device)
         self.stream = torch.cuda.Stream(self.device)
+        self.copy_stream = torch.cuda.Stream(self.device)
+        self.chunks = max(1, int(chunks))
         self._bufs = {}
 
     def _buf(self, name, like: torch.Tensor):
@@ -104,16 +110,50 @@ class HostDecoder:
             self._bufs[name] = b
         return b[: like.numel()].view(like.shape)
 
+    def _groups(self, ip: list, rows: int):
+        B = len(ip) - 1
+        ok = all(0 <= ip[i] <= ip[i + 1] <= rows for i in range(B))
+        if not ok or self.chunks == 1 or B < 2:
+            return [(0, B, 0, rows)]
+        total = ip[B] - ip[0]
+        groups, c0 = [], 0
+        for c in range(1, self.chunks + 1):
+            target = ip[0] + total * c // self.chunks
+            c1 = c0 + 1
+            while c1 < B and ip[c1] < target:
+                c1 += 1
+            if c == self.chunks:
+                c1 = B
+            if c1 > c0:
+                groups.append((c0, c1, ip[c0], ip[c1]))
+                c0 = c1
+            if c0 >= B:
+                break
+        return groups
+
     def __call__(self, q, kv_packed, kv_scale, kv_indptr, sm_scale, out_host: torch.Tensor) -> torch.Tensor:
-        with torch.cuda.stream(self.stream):
-            dq = self._buf("q", q).copy_(q, non_blocking=True)
-            dkv = self._buf("kv", kv_packed).copy_(kv_packed, non_blocking=True)
-            dsc = self._buf("sc", kv_scale).copy_(kv_scale, non_blocking=True)
-            dip = self._buf("ip", kv_indptr).copy_(kv_indptr, non_blocking=True)
-            dout = self._buf("out", out_host)
-            decode(dq, dkv, dsc, dip, sm_scale, out=dout, stream=self.stream)
-            out_host.copy_(dout, non_blocking=True)
+        dq, dkv, dsc = self._buf("q", q), self._buf("kv", kv_packed), self._buf("sc", kv_scale)
+        dip, dout = self._buf("ip", kv_indptr), self._buf("out", out_host)
+        ip = kv_indptr.tolist()
+        groups = self._groups(ip, kv_packed.shape[0])
+        cs, ms = self.copy_stream, self.stream
+        cs.wait_stream(ms)  # buffers are reused across calls
+        with torch.cuda.stream(cs):
+            dip.copy_(kv_indptr, non_blocking=True)
+        for c0, c1, r0, r1 in groups:
+            with torch.cuda.stream(cs):
+                dq[c0:c1].copy_(q[c0:c1], non_blocking=True)
+                if r1 > r0:
+                    dkv[r0:r1].copy_(kv_packed[r0:r1], non_blocking=True)
+                    dsc[r0:r1].copy_(kv_scale[r0:r1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+            ms.wait_event(ev)
+            with torch.cuda.stream(ms):
+                decode(dq[c0:c1], dkv, dsc, dip[c0:c1 + 1], sm_scale, out=dout[c0:c1], stream=ms)
+                out_host[c0:c1].copy_(dout[c0:c1], non_blocking=True)
         return out_host
 
     def synchronize(self):
+        self.copy_stream.synchronize()
         self.stream.synchronize()

@@ -208,3 +208,22 @@ def test_malformed_indptr_is_flagged_and_in_bounds():
     assert st & 1
     ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, torch.tensor([0, 20, 20], dtype=torch.int32), d.sm_scale)
     check_close(as64(out), ref, "clamped")
+
+
+def test_host_decoder_chunked_pipeline_matches_device_decode():
+    """End-to-end path from pinned host buffers, cut into groups of sequences whose
+    copies overlap the previous group's decode: same result as one device decode."""
+    from mla_decode_attention_mxfp4_gb300 import HostDecoder
+    d = MI.make_custom([700, 0, 1500, 33, 2600, 1, 0, 900, 4100], seed=77)
+    dev = torch.device("cuda:0")
+    ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale)
+    hq, hkv, hsc, hip = (d.q.pin_memory(), d.kv_packed.pin_memory(), d.kv_scale.pin_memory(),
+                         d.kv_indptr.pin_memory())
+    for chunks in (1, 3, 8):
+        hd = HostDecoder(dev, chunks=chunks)
+        hout = torch.empty(d.batch, 16, 512, dtype=torch.bfloat16).pin_memory()
+        for _ in range(2):  # the second call reuses the device buffers
+            hout.fill_(float("nan"))
+            hd(hq, hkv, hsc, hip, d.sm_scale, hout)
+            hd.synchronize()
+            check_close(as64(hout), ref, f"host decoder, {chunks} groups")
