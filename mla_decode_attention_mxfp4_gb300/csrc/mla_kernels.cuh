@@ -134,16 +134,18 @@ constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229
 constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] output factors
 constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229664: [4 warps][16 m, 16 alpha]
 constexpr int kOffSt = kOffMst + 4 * 2 * kHeads * 4;                      // 230176: [2][128] token exponents
-constexpr int kOffTmem = kOffSt + 2 * kTile * 4;                          // 231200
-constexpr int kOffBar = kOffTmem + 16;                                    // 231216
+constexpr int kOffStq = kOffSt + 2 * kTile * 4;                           // 231200: [2][128] S_t within a quarter
+constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 232224
+constexpr int kOffBar = kOffTmem + 16;                                    // 232240
 constexpr int kNumBars = 16;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231344
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 232368
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
 constexpr uint32_t kBarSm = 1;     // named barrier of the softmax group
 constexpr uint32_t kBarAll = 2;    // dequant + softmax groups + MMA warp
 constexpr uint32_t kBarDq = 3;     // named barrier of the dequant group
+constexpr uint32_t kBarStq = 4;    // 4 + 4 * (tile parity) + lane quarter: S_t hand-off in a quarter
 
 struct SplitParams {
   const __nv_bfloat16* q;
@@ -394,26 +396,37 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
 }
 
 // K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
-// s_tb >= S_t - 15 (the truncated high byte of an f16 with <= 2 significant bits).
-// Token t = this thread's lane of the quarter; blocks b == part (mod kDqParts), software
-// pipelined (the next block's bytes are loaded while this one is converted).
-// Returns S_t (0 for tokens past the tile).
-__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane) {
+// s_tb >= S_t - 14; blocks further below the token's largest are zero (their elements
+// are under 2^-13 of the token's maximum).  Token t = this thread's lane of the
+// quarter; blocks b == part (mod kDqParts), software pipelined (the next block's bytes
+// are loaded while this one is converted).  Part 0 finds S_t and hands it to the
+// quarter's other parts through stq and a named barrier.  Returns S_t (0 for tokens
+// past the tile).
+__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
+                                              int* stq, uint32_t bar_id) {
   const bool valid = t < n;
   const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)t0 * kNScale) & 15) + t * kNScale;
   int St = 0;
-  if (valid) {
-    // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
-    // high byte of the largest 16-bit word
-    uint32_t mhi = 0, mlo = 0;
+  if (part == 0) {
+    if (valid) {
+      // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
+      // high byte of the largest 16-bit word
+      uint32_t mhi = 0, mlo = 0;
 #pragma unroll
-    for (int i = 0; i < kNScale / 2; ++i) {
-      const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
-      mhi = max(mhi, two);
-      mlo = max(mlo, two & 0xFFu);
+      for (int i = 0; i < kNScale / 2; ++i) {
+        const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
+        mhi = max(mhi, two);
+        mlo = max(mlo, two & 0xFFu);
+      }
+      St = (int)max(mhi >> 8, mlo);
     }
-    St = (int)max(mhi >> 8, mlo);
+    stq[t] = St;
+    named_arrive(bar_id, 32 * kDqParts);
+  } else {
+    named_sync(bar_id, 32 * kDqParts);
+    St = stq[t];
   }
+  const int sbias = 15 - St;  // f16 exponent field of 2^(s - S_t) is s + sbias when positive
   const uint8_t* row = st + t * kPacked + 16 * part;
   const uint8_t* sbp = sb + part;
   constexpr int kNb = (kNScale + kDqParts - 1) / kDqParts;  // blocks per part (the last ones may be absent)
@@ -429,7 +442,7 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
       wn = *reinterpret_cast<const uint4*>(row + 16 * kDqParts * (j + 1));
       sn = valid ? (int)sbp[kDqParts * (j + 1)] : 0;
     }
-    const uint32_t f2 = valid ? f16x2_pow2(s - St) : 0u;
+    const uint32_t f2 = valid ? (uint32_t)max(s + sbias, 0) * 0x04000400u : 0u;
     uint32_t e[8];
     chunk_to_e5m2(w, f2, e);
     tmem_st8(a_lane + 8 * (part + kDqParts * j), e);
@@ -624,7 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     wait_or_flag(&bar_full[0], 0, p, aborted);
     build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
     if (gtid == 0) mbar_arrive(bar_qempty);
-    int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA);
+    int* stq = reinterpret_cast<int*>(smem + kOffStq);  // [2][128]
+    int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, stq, kBarStq + q4);
     tc_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -653,7 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         }
         tc_fence_after();
         St_next = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, nx.t0, nx.n, t, part,
-                                 t_lane + kColA + kColsA * ((k + 1) & 1));
+                                 t_lane + kColA + kColsA * ((k + 1) & 1), stq + ((k + 1) & 1) * kTile,
+                                 kBarStq + 4 * ((k + 1) & 1) + q4);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
