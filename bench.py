@@ -373,7 +373,7 @@ def run_native(args):
         "us_per_call_graph": graph_ms * 1e3 if isinstance(graph_ms, float) else graph_ms,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic",
+        "dtype": "fp8", "data": "synthetic",
         "config": dict(_workload_desc(args.workload, d),
                        l2=f"timed calls rotate over {copies} input copies "
                           f"({copies * in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES // 2**20} MiB)",
