@@ -108,6 +108,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;      // 2 x 144 columns: e5m2 K tile, column c = dims 4c..4c+3
 constexpr uint32_t kColsA = 144;
 constexpr uint32_t kColS = 288;    // 2 x 32 columns: S^T from the hi (0..15) and lo (16..31) query parts
+constexpr uint32_t kColSt = 352;   // 4 columns: S_t of the tile's tokens (tile k in column k % 4)
 constexpr uint32_t kColO = 384;    // 128 columns: O^T, 4 blocks of 128 dims x (16 hi + 16 lo P parts)
 
 // Qhat, e4m3 hi (n = head) and lo (n = 16 + head) parts, K-major without swizzle:
@@ -133,11 +134,10 @@ constexpr int kOffEh = kOffCh + 4 * kHeads * 4;                           // 229
 constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229344: [16 heads][4 quarters]
 constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] output factors
 constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229664: [4 warps][16 m, 16 alpha]
-constexpr int kOffSt = kOffMst + 4 * 2 * kHeads * 4;                      // 230176: [2][128] token exponents
-constexpr int kOffStq = kOffSt + 2 * kTile * 4;                           // 231200: [2][128] S_t within a quarter
-constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 232224
+constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230176: [2][128] S_t within a quarter
+constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231200
 constexpr int kOffBar = kOffTmem + 16;                                    // 232240
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 14;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 232368
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
@@ -398,12 +398,13 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
 // K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
 // s_tb >= S_t - 14; blocks further below the token's largest are zero (their elements
 // are under 2^-13 of the token's maximum).  Token t = this thread's lane of the
-// quarter; blocks b == part (mod kDqParts), software pipelined (the next block's bytes
-// are loaded while this one is converted).  Part 0 finds S_t and hands it to the
-// quarter's other parts through stq and a named barrier.  Returns S_t (0 for tokens
-// past the tile).
-__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
-                                              int* stq, uint32_t bar_id) {
+// quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
+// pair's bytes are loaded while this pair is converted; one 16-column store per pair).
+// Part 0 finds S_t, hands it to the quarter's other parts through stq and a named
+// barrier, and stores it in tensor-memory column st_col for the softmax group (0 for
+// tokens past the tile).
+__device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
+                                               uint32_t st_col, int* stq, uint32_t bar_id) {
   const bool valid = t < n;
   const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)t0 * kNScale) & 15) + t * kNScale;
   int St = 0;
@@ -422,32 +423,36 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, 
     }
     stq[t] = St;
     named_arrive(bar_id, 32 * kDqParts);
+    const uint32_t sv[1] = {(uint32_t)St};
+    tmem_st1(st_col, sv);
   } else {
     named_sync(bar_id, 32 * kDqParts);
     St = stq[t];
   }
-  const int sbias = 15 - St;  // f16 exponent field of 2^(s - S_t) is s + sbias when positive
-  const uint8_t* row = st + t * kPacked + 16 * part;
-  const uint8_t* sbp = sb + part;
-  constexpr int kNb = (kNScale + kDqParts - 1) / kDqParts;  // blocks per part (the last ones may be absent)
-  uint4 wn = *reinterpret_cast<const uint4*>(row);
-  int sn = valid ? (int)sbp[0] : 0;
-  // unrolled by two only: the warp roles of a CTA share the instruction caches
-#pragma unroll 2
-  for (int j = 0; j < kNb; ++j) {
-    if (part + kDqParts * j >= kNScale) break;
-    const uint4 w = wn;
-    const int s = sn;
-    if (j + 1 < kNb && part + kDqParts * (j + 1) < kNScale) {
-      wn = *reinterpret_cast<const uint4*>(row + 16 * kDqParts * (j + 1));
-      sn = valid ? (int)sbp[kDqParts * (j + 1)] : 0;
+  constexpr int kNb = kNScale / kDqParts;  // consecutive blocks b0 .. b0 + kNb - 1 of this part
+  static_assert(kNScale % kDqParts == 0 && kNb % 2 == 0, "pairs of blocks per part");
+  const int b0 = part * kNb;
+  const int sbias = valid ? 15 - St : -1024;  // f16 exponent field of 2^(s - S_t) is s + sbias when positive
+  const uint8_t* row = st + t * kPacked + 16 * b0;
+  const uint8_t* sp = sb + b0;
+  uint4 wa = *reinterpret_cast<const uint4*>(row), wb = *reinterpret_cast<const uint4*>(row + 16);
+  int sa = sp[0], sc = sp[1];
+  // not unrolled: the warp roles of a CTA share the instruction caches
+#pragma unroll 1
+  for (int j = 0; j < kNb; j += 2) {
+    const uint4 xa = wa, xb = wb;
+    const int ta = sa, tb = sc;
+    if (j + 2 < kNb) {
+      wa = *reinterpret_cast<const uint4*>(row + 16 * j + 32);
+      wb = *reinterpret_cast<const uint4*>(row + 16 * j + 48);
+      sa = sp[j + 2];
+      sc = sp[j + 3];
     }
-    const uint32_t f2 = valid ? (uint32_t)max(s + sbias, 0) * 0x04000400u : 0u;
-    uint32_t e[8];
-    chunk_to_e5m2(w, f2, e);
-    tmem_st8(a_lane + 8 * (part + kDqParts * j), e);
+    uint32_t e[16];
+    chunk_to_e5m2(xa, (uint32_t)max(ta + sbias, 0) * 0x04000400u, *reinterpret_cast<uint32_t(*)[8]>(&e[0]));
+    chunk_to_e5m2(xb, (uint32_t)max(tb + sbias, 0) * 0x04000400u, *reinterpret_cast<uint32_t(*)[8]>(&e[8]));
+    tmem_st16(a_lane + 8 * (b0 + j), e);
   }
-  return St;
 }
 
 // Maximum (kMax) or sum over the 32 lanes of sixteen per-lane values; lane L ends
@@ -500,10 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bar_qempty = bars + 6;    // query rows consumed (one per segment)
   uint64_t* bar_kready = bars + 7;    // [2] K tile in tensor-memory buffer b, and its Qhat, ready (dequant group)
   uint64_t* bar_vready = bars + 9;    // V^T of a tile in shared memory (dequant group)
-  uint64_t* bar_stready = bars + 10;  // [2] token exponents of a tile published (dequant group)
-  uint64_t* bar_pready = bars + 12;   // P^T and any O^T rescale of a tile done (softmax group)
-  uint64_t* bar_qk = bars + 13;       // [2] S^T buffer b written (MMA commit)
-  uint64_t* bar_pv = bars + 15;       // P.V of a tile completed (MMA commit)
+  uint64_t* bar_pready = bars + 10;   // P^T and any O^T rescale of a tile done (softmax group)
+  uint64_t* bar_qk = bars + 11;       // [2] S^T buffer b and the tile's S_t written (MMA commit)
+  uint64_t* bar_pv = bars + 13;       // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -513,8 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     mbar_init(&bar_kready[0], kDqWarps);
     mbar_init(&bar_kready[1], kDqWarps);
     mbar_init(bar_vready, kDqWarps);
-    mbar_init(&bar_stready[0], kDqWarps);
-    mbar_init(&bar_stready[1], kDqWarps);
     mbar_init(bar_pready, kSmWarps);
     mbar_init(&bar_qk[0], 1);
     mbar_init(&bar_qk[1], 1);
@@ -623,12 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   const int q4 = warp & 3;
   const int t = q4 * 32 + lane;  // token of the tile = tensor-memory lane
   const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-  int* st_buf = reinterpret_cast<int*>(smem + kOffSt);  // [2][128]
 
   if (warp >= kDqWarp0) {
     // ======================= dequant group (warps 6..17) ========================
     // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
-    // Warp (q4, part) owns tokens 32*q4.. and K/V blocks b == part (mod kDqParts).
+    // Warp (q4, part) owns tokens 32*q4.., K blocks 6*part .. 6*part+5 and V blocks
+    // b == part (mod kDqParts).
     const int dwarp = warp - kDqWarp0;  // 0..7
     const int part = dwarp >> 2;
     const int gtid = tid - kDqWarp0 * 32;  // 0..383
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
     if (gtid == 0) mbar_arrive(bar_qempty);
     int* stq = reinterpret_cast<int*>(smem + kOffStq);  // [2][128]
-    int St_next = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, stq, kBarStq + q4);
+    k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, t_lane + kColSt, stq, kBarStq + q4);
     tc_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -646,29 +648,29 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       mbar_arrive(&bar_kready[0]);
       mbar_arrive(&bar_empty[0]);
     }
-    if (part == 0) st_buf[t] = St_next;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar_stready[0]);
     int k = 0;
     bool has_next;
     do {
-      TileIter nx = it;
-      has_next = nx.next();
+      has_next = it.next();  // it: tile k+1 from here on (the V^T step below needs only k)
       if (has_next) {
-        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed ----
+        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed:
+        // for k >= 2 that is implied by the completion of P.V of tile k-2, which the MMA warp issued
+        // after QK^T of tile k-1 and which this group waited for in the previous iteration ----
         const int s1 = (k + 1) % kStages;
         wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
-        if (k >= 1) wait_or_flag(&bar_qk[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
-        if (nx.first) {
+        if (k == 1) wait_or_flag(&bar_qk[0], 0, p, aborted);
+        if (it.first) {
           // the next segment's Qhat replaces this one once QK^T of tile k has completed
           wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
-          build_qhat(smem, p.sm_scale, nx.seg & 3, gtid, dwarp, lane);
+          build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
           if (gtid == 0) mbar_arrive(bar_qempty);
         }
         tc_fence_after();
-        St_next = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, nx.t0, nx.n, t, part,
-                                 t_lane + kColA + kColsA * ((k + 1) & 1), stq + ((k + 1) & 1) * kTile,
-                                 kBarStq + 4 * ((k + 1) & 1) + q4);
+        // S_t of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3, which
+        // finished before P.V of tile k-3 (waited for two iterations ago)
+        k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.t0, it.n, t, part,
+                       t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
+                       stq + ((k + 1) & 1) * kTile, kBarStq + 4 * ((k + 1) & 1) + q4);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -709,14 +711,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_vready);
-      // ---- publish the token exponents of tile k+1 (the softmax of tile k-1, which used
-      // this buffer, finished before P.V of tile k-1) ----
-      if (has_next) {
-        if (part == 0) st_buf[((k + 1) & 1) * kTile + t] = St_next;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_stready[(k + 1) & 1]);
-      }
-      it = nx;
       ++k;
     } while (has_next);
   } else {
@@ -732,32 +726,43 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     int k = 0;
     bool has_next;
     do {
-      TileIter nx = it;
-      has_next = nx.next();
       const bool valid = t < it.n;
       const bool seg_first = it.first;
-      wait_or_flag(&bar_stready[k & 1], (k >> 1) & 1, p, aborted);
-      const int St = st_buf[(k & 1) * kTile + t];
       const float* ch = chs + (it.seg & 3) * kHeads;
-      const float stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
+      // S^T and the tile's token exponents S_t (stored by the dequant group before the K tile
+      // that QK^T read was declared ready)
       wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
       tc_fence_after();
+      int St;
+      float stok;
       float s2[16];
       float* hmax = reinterpret_cast<float*>(smem + kOffHmax) + (k & 1) * 4 * kHeads;  // [16 heads][4 quarters]
       int* rwb = reinterpret_cast<int*>(smem + kOffRw) + (k & 1) * 4;
       {
-        uint32_t rh[16], rl[16];
+        uint32_t rh[16], rl[16], sv[1];
         const uint32_t scol = t_lane + kColS + 32 * (k & 1);
         tmem_ld16_nowait(scol, rh);
         tmem_ld16_nowait(scol + 16, rl);
+        tmem_ld1_nowait(t_lane + kColSt + (k & 3), sv);
         tc_wait_ld();
+        St = valid ? (int)sv[0] : 0;
+        stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
+        // s = (hi + lo part scores) * (head factor * token factor); -inf past the tile's tokens
+        const float2 st2 = make_float2(stok, stok);
+        const float pen = valid ? 0.f : -INFINITY;
+        const float2 pen2 = make_float2(pen, pen);
 #pragma unroll
         for (int i = 0; i < 16; i += 4) {
           const float4 c4 = *reinterpret_cast<const float4*>(ch + i);
-          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            s2[i + u] = valid ? (__uint_as_float(rh[i + u]) + __uint_as_float(rl[i + u])) * (cc[u] * stok) : -INFINITY;
+          for (int u = 0; u < 4; u += 2) {
+            const float2 cs = f2mul(u == 0 ? make_float2(c4.x, c4.y) : make_float2(c4.z, c4.w), st2);
+            const float2 sum = f2add(make_float2(__uint_as_float(rh[i + u]), __uint_as_float(rh[i + u + 1])),
+                                     make_float2(__uint_as_float(rl[i + u]), __uint_as_float(rl[i + u + 1])));
+            const float2 sv2 = f2fma(sum, cs, pen2);
+            s2[i + u] = sv2.x;
+            s2[i + u + 1] = sv2.y;
+          }
         }
         const float wm = warp_reduce16<true>(s2, lane);
         if ((lane & 1) == 0) hmax[(lane >> 1) * 4 + q4] = wm;
@@ -803,23 +808,26 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         alpha_v[i] = b.x; alpha_v[i + 1] = b.y; alpha_v[i + 2] = b.z; alpha_v[i + 3] = b.w;
       }
       const float ptok = valid ? exp2i(St - Rnew) : 0.f;
+      const float2 ptok2 = make_float2(ptok, ptok);
       uint32_t phi[4], plo[4];
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        float pp[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float pv = ex2(s2[i + u] - m_now[i + u]);
-          l_part[i + u] = seg_first ? pv : l_part[i + u] * alpha_v[i + u] + pv;
-          pp[u] = pv * ptok;
-        }
-        // P = hi + lo, both e4m3
+        const float2 d = f2sub(make_float2(s2[i], s2[i + 1]), make_float2(m_now[i], m_now[i + 1]));
+        const float2 pv = make_float2(ex2(d.x), ex2(d.y));
+        const float2 lp = make_float2(l_part[i], l_part[i + 1]);
+        const float2 ln = seg_first ? pv : f2fma(lp, make_float2(alpha_v[i], alpha_v[i + 1]), pv);
+        l_part[i] = ln.x;
+        l_part[i + 1] = ln.y;
+        const float2 pp = f2mul(pv, ptok2);
+        // P = hi + lo, both e4m3, split in f16 (P <= 2^8: the f16 rounding is 2^-11 relative and
+        // pp16 - hi is exact in f16)
+        const __half2 p16 = __floats2half2_rn(pp.x, pp.y);
         const __nv_fp8x2_storage_t hi2 =
-            __nv_cvt_float2_to_fp8x2(make_float2(pp[0], pp[1]), __NV_SATFINITE, __NV_E4M3);
+            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&p16), __NV_SATFINITE, __NV_E4M3);
         const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
-        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __half2 rest = __hsub2(p16, *reinterpret_cast<const __half2*>(&hr));
         const __nv_fp8x2_storage_t lo2 =
-            __nv_cvt_float2_to_fp8x2(make_float2(pp[0] - hf.x, pp[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
+            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rest), __NV_SATFINITE, __NV_E4M3);
         if ((i & 2) == 0) {
           phi[i >> 2] = (uint32_t)hi2;
           plo[i >> 2] = (uint32_t)lo2;
@@ -838,21 +846,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       tc_fence_after();
       if (resc) {
         const float rs = exp2i(R - Rnew);
+        // eight columns at a time (column 8q + i holds head (8q + i) % 16): few live registers
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
-          uint32_t a[16], c[16];
           const uint32_t col = t_lane + kColO + 32 * blk;
-          tmem_ld16_nowait(col, a);
-          tmem_ld16_nowait(col + 16, c);
-          tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float f = alpha_v[i] * rs;
-            a[i] = __float_as_uint(__uint_as_float(a[i]) * f);
-            c[i] = __float_as_uint(__uint_as_float(c[i]) * f);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t a[8];
+            tmem_ld8_nowait(col + 8 * q, a);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = __float_as_uint(__uint_as_float(a[i]) * (alpha_v[(8 * q + i) & 15] * rs));
+            tmem_st8(col + 8 * q, a);
           }
-          tmem_st16(col, a);
-          tmem_st16(col + 16, c);
         }
         tc_wait_st();
       }
@@ -910,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         tc_fence_before();
         named_sync(kBarSm, kSmThreads);  // lw, ofac and the accumulator are reused by the next segment
       }
-      it = nx;
+      has_next = it.next();
       ++k;
     } while (has_next);
   }
