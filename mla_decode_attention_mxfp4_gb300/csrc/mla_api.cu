@@ -120,10 +120,35 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   sp.B = batch;
   sp.sm_scale = sm_scale;
   sp.timeout_ns = 1000000000ull;
+  // split and merge are launched with programmatic stream serialization: each may be
+  // scheduled while its predecessor runs and waits for it with griddepcontrol.wait.  The
+  // timed variant records events between the launches, which orders them as usual.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  mla::mla_split_kernel<<<di.grid, mla::kThreads, mla::kSmemBytes, stream>>>(sp);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(di.grid);
+    cfg.blockDim = dim3(mla::kThreads);
+    cfg.dynamicSmemBytes = mla::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::mla_split_kernel, sp) != cudaSuccess) return MLA_ERR_CUDA;
+  }
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  mla::mla_merge_kernel<<<batch, mla::kMergeThreads, 0, stream>>>(static_cast<__nv_bfloat16*>(out), w, batch);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(batch);
+    cfg.blockDim = dim3(mla::kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::mla_merge_kernel, static_cast<__nv_bfloat16*>(out), w, batch) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

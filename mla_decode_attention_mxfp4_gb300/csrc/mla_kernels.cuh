@@ -241,6 +241,7 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tot, int& t
 // kv_null: the KV buffers are absent (NULL), so no row may be read.
 __global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
                                                              int G, int kv_null, Workspace ws) {
+  grid_launch_dependents();  // the split kernel's prologue may run alongside
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_ipc[kPartSmemSeqs + 1];  // copy of ipc for batch <= kPartSmemSeqs
@@ -494,10 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
-  const int* meta = p.ws.meta;
-  const int geff = meta[kMetaGeff];
-  if (g >= geff) return;
-  const int per = meta[kMetaPer];
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_full = bars;          // [3] stage landed (producer, tx bytes)
@@ -523,18 +520,26 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     mbar_init(bar_pv, 1);
     fence_barrier_init();
   }
-  __syncthreads();
-
-  TileIter it;
-  const bool any = it.init(p.ws.ipc, p.B, g, per, p.ws.cta_first[g]);
-  if (!any) return;  // cannot happen for g < geff
-  bool aborted = false;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  // Everything above overlaps the partition kernel (programmatic dependent launch); its
+  // results are read from here on.  The merge kernel may be scheduled from now on: it waits
+  // for this grid's completion itself.
+  grid_dependency_wait();
+  grid_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int* meta = p.ws.meta;
+  const int geff = meta[kMetaGeff];
+  const int per = meta[kMetaPer];
+  TileIter it;
+  if (g >= geff || !it.init(p.ws.ipc, p.B, g, per, p.ws.cta_first[g])) {  // the latter cannot happen for g < geff
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  bool aborted = false;
 
   // =========================== producer warp ===================================
   if (warp == kProdWarp) {
@@ -931,6 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 constexpr int kMergeThreads = 32 * kHeads;
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws,
                                                                   int B) {
+  grid_dependency_wait();  // the split kernel's partials
   const int b = blockIdx.x;
   if (b >= B) return;
   const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
