@@ -769,56 +769,76 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
             s2[i + u + 1] = sv2.y;
           }
         }
-        const float wm = warp_reduce16<true>(s2, lane);
-        if ((lane & 1) == 0) hmax[(lane >> 1) * 4 + q4] = wm;
       }
-      const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
-      if (lane == 0) rwb[q4] = rw;
-      named_sync(kBarSm, kSmThreads);
-      // running statistics: lane L computes head L >> 1; the lane pair agrees
-      int Rnew;
-      bool resc;
-      {
-        const int4 rwv = *reinterpret_cast<const int4*>(rwb);
-        const int Rtile = max(max(rwv.x, rwv.y), max(rwv.z, rwv.w));
-        Rnew = seg_first ? Rtile : (Rtile > R + kMaxThresh ? Rtile : R);
-        const int h = lane >> 1;
-        const float4 hm = *reinterpret_cast<const float4*>(hmax + h * 4);
-        const float M = fmaxf(fmaxf(hm.x, hm.y), fmaxf(hm.z, hm.w));
-        const float mo = mstate[h];
-        float mn = mo, alpha = 1.f;
-        bool moved = false;
-        if (seg_first) {
-          mn = M;
-          alpha = 0.f;
-        } else if (M > mo + (float)kMaxThresh) {
-          mn = M;
-          alpha = ex2(mo - M);
-          moved = true;
-        }
-        resc = __any_sync(0xffffffffu, moved) || (!seg_first && Rnew != R);
-        __syncwarp();
-        if ((lane & 1) == 0) {
-          mstate[h] = mn;
-          mstate[kHeads + h] = alpha;
-        }
-        __syncwarp();
-      }
-      float m_now[16], alpha_v[16];
+      // d = s - m with the running maxima as they stand.  When every score of the tile is
+      // within kMaxThresh of its head's maximum and every token exponent within kMaxThresh
+      // of R (one AND-reducing barrier over the group), nothing moves: no tile maxima are
+      // exchanged and P uses d as it is.  A moving maximum or a segment start takes the
+      // full path (the same decisions either way).
+      float d[16], alpha_v[16];
+      float dmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
         const float4 a = *reinterpret_cast<const float4*>(mstate + i);
-        const float4 b = *reinterpret_cast<const float4*>(mstate + kHeads + i);
-        m_now[i] = a.x; m_now[i + 1] = a.y; m_now[i + 2] = a.z; m_now[i + 3] = a.w;
-        alpha_v[i] = b.x; alpha_v[i + 1] = b.y; alpha_v[i + 2] = b.z; alpha_v[i + 3] = b.w;
+        const float2 d0 = f2sub(make_float2(s2[i], s2[i + 1]), make_float2(a.x, a.y));
+        const float2 d1 = f2sub(make_float2(s2[i + 2], s2[i + 3]), make_float2(a.z, a.w));
+        d[i] = d0.x; d[i + 1] = d0.y; d[i + 2] = d1.x; d[i + 3] = d1.y;
+        dmax = fmaxf(dmax, fmaxf(fmaxf(d0.x, d0.y), fmaxf(d1.x, d1.y)));
+        alpha_v[i] = alpha_v[i + 1] = alpha_v[i + 2] = alpha_v[i + 3] = 1.f;
+      }
+      const bool fits = !seg_first && dmax <= (float)kMaxThresh && (!valid || St <= R + kMaxThresh);
+      int Rnew = R;
+      bool resc = false;
+      if (!named_sync_and(kBarSm, kSmThreads, fits)) {
+        // tile maxima: per head over the warp's tokens, then over the four warps
+        const float wm = warp_reduce16<true>(s2, lane);
+        if ((lane & 1) == 0) hmax[(lane >> 1) * 4 + q4] = wm;
+        const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
+        if (lane == 0) rwb[q4] = rw;
+        named_sync(kBarSm, kSmThreads);
+        // running statistics: lane L computes head L >> 1; the lane pair agrees
+        {
+          const int4 rwv = *reinterpret_cast<const int4*>(rwb);
+          const int Rtile = max(max(rwv.x, rwv.y), max(rwv.z, rwv.w));
+          Rnew = seg_first ? Rtile : (Rtile > R + kMaxThresh ? Rtile : R);
+          const int h = lane >> 1;
+          const float4 hm = *reinterpret_cast<const float4*>(hmax + h * 4);
+          const float M = fmaxf(fmaxf(hm.x, hm.y), fmaxf(hm.z, hm.w));
+          const float mo = mstate[h];
+          float mn = mo, alpha = 1.f;
+          bool moved = false;
+          if (seg_first) {
+            mn = M;
+            alpha = 0.f;
+          } else if (M > mo + (float)kMaxThresh) {
+            mn = M;
+            alpha = ex2(mo - M);
+            moved = true;
+          }
+          resc = __any_sync(0xffffffffu, moved) || (!seg_first && Rnew != R);
+          __syncwarp();
+          if ((lane & 1) == 0) {
+            mstate[h] = mn;
+            mstate[kHeads + h] = alpha;
+          }
+          __syncwarp();
+        }
+  #pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(mstate + i);
+          const float4 b = *reinterpret_cast<const float4*>(mstate + kHeads + i);
+          const float2 d0 = f2sub(make_float2(s2[i], s2[i + 1]), make_float2(a.x, a.y));
+          const float2 d1 = f2sub(make_float2(s2[i + 2], s2[i + 3]), make_float2(a.z, a.w));
+          d[i] = d0.x; d[i + 1] = d0.y; d[i + 2] = d1.x; d[i + 3] = d1.y;
+          alpha_v[i] = b.x; alpha_v[i + 1] = b.y; alpha_v[i + 2] = b.z; alpha_v[i + 3] = b.w;
+        }
       }
       const float ptok = valid ? exp2i(St - Rnew) : 0.f;
       const float2 ptok2 = make_float2(ptok, ptok);
       uint32_t phi[4], plo[4];
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        const float2 d = f2sub(make_float2(s2[i], s2[i + 1]), make_float2(m_now[i], m_now[i + 1]));
-        const float2 pv = make_float2(ex2(d.x), ex2(d.y));
+        const float2 pv = make_float2(ex2(d[i]), ex2(d[i + 1]));
         const float2 lp = make_float2(l_part[i], l_part[i + 1]);
         const float2 ln = seg_first ? pv : f2fma(lp, make_float2(alpha_v[i], alpha_v[i + 1]), pv);
         l_part[i] = ln.x;
