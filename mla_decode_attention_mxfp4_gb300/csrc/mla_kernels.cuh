@@ -971,6 +971,16 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16*
   const int ns = si.y - si.x + 1;
   if (ns < 2) return;  // written by the split kernel
   const int base = si.z;
+  // the first two partials' rows are requested together with the weights (one round trip
+  // to L2 for the common two-way split)
+  const float4* p0 = reinterpret_cast<const float4*>(ws.part_acc + ((long long)base * kHeads + h) * kDv + lane * 16);
+  const float4* p1 = p0 + kHeads * kDv / 4;
+  float4 y0[4], y1[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    y0[q] = p0[q];
+    y1[q] = ns > 1 ? p1[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // lane i holds the weight of partials i, i+32, ...; M over all partials first
   float M = -INFINITY;
   for (int i = lane; i < ns; i += 32) M = fmaxf(M, ws.part_lse[(base + i) * kHeads + h]);
@@ -993,8 +1003,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16*
       float4 x0[4], x1[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        x0[q] = s0[q];
-        x1[q] = s1[q];
+        x0[q] = c0 + i == 0 ? y0[q] : s0[q];
+        x1[q] = c0 + i == 0 ? y1[q] : s1[q];
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
