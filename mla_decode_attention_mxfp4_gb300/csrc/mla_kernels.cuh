@@ -92,7 +92,7 @@ struct Workspace {
   int* meta;          // [16]
   int* ipc;           // [B+1] sanitised indptr
   int4* seqinfo;      // [B]: first range, last range, partial slot base, -
-  int* cta_first;     // [G]: first sequence overlapping range g
+  int4* cta_desc;     // [G][2]: range g = {r0, r1, first sequence b, ipc[b]}, {ipc[b+1], -, -, -}
   float* part_lse;    // [2G][16]   log2-sum-exp of each partial
   float* part_acc;    // [2G][16][512] normalised partial output
 };
@@ -169,19 +169,16 @@ struct TileIter {
   int seg;     // segment counter
   bool first, last;
 
-  __device__ bool init(const int* ipc_, int B_, int g, int per, int first_seq) {
+  // d0 = {r0, r1, first sequence b, ipc[b]}, d1.x = ipc[b+1] (written by the partition kernel)
+  __device__ bool init(const int* ipc_, int B_, int4 d0, int4 d1) {
     ipc = ipc_;
     B = B_;
-    const int rbase = ipc[0];
-    const int rend = ipc[B];
-    const long long r0ll = (long long)rbase + (long long)g * per;
-    if (r0ll >= rend) return false;
-    const int r0 = (int)r0ll;
-    r1 = (int)min((long long)rend, r0ll + per);
-    b = first_seq;
-    const int sb = ipc[b];
-    t0 = max(r0, sb);
-    s1 = min(r1, ipc[b + 1]);
+    const int r0 = d0.x;
+    r1 = d0.y;
+    if (r0 >= r1) return false;
+    b = d0.z;
+    t0 = max(r0, d0.w);
+    s1 = min(r1, d1.x);
     n = min(kTile, s1 - t0);
     seg = 0;
     first = true;
@@ -294,16 +291,23 @@ __global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __re
     if (b < B) ws.seqinfo[b] = make_int4(f, l, run + incl - contrib, 0);
     run += tot;
   }
-  // first sequence of each range: largest b with ipc[b] <= r0
-  for (int g = tid; g < geff; g += 1024) {
-    const int r0 = rbase + g * per;
-    int lo = 0, hi2 = B - 1;
-    while (lo < hi2) {
-      const int mid = (lo + hi2 + 1) >> 1;
-      if (ipc[mid] <= r0) lo = mid;
-      else hi2 = mid - 1;
+  // per range: its rows, its first sequence (largest b with ipc[b] <= r0) and that
+  // sequence's rows, so a CTA starts from one 32-byte load; empty ranges have r0 == r1
+  for (int g = tid; g < G; g += 1024) {
+    int4 d0 = make_int4(0, 0, 0, 0), d1 = make_int4(0, 0, 0, 0);
+    if (g < geff) {
+      const int r0 = rbase + g * per;
+      int lo = 0, hi2 = B - 1;
+      while (lo < hi2) {
+        const int mid = (lo + hi2 + 1) >> 1;
+        if (ipc[mid] <= r0) lo = mid;
+        else hi2 = mid - 1;
+      }
+      d0 = make_int4(r0, (int)min((long long)ipc[B], (long long)r0 + per), lo, ipc[lo]);
+      d1.x = ipc[lo + 1];
     }
-    ws.cta_first[g] = lo;
+    ws.cta_desc[2 * g] = d0;
+    ws.cta_desc[2 * g + 1] = d1;
   }
   if (tid == 0) {
     ws.meta[kMetaN] = N;
@@ -531,11 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int* meta = p.ws.meta;
-  const int geff = meta[kMetaGeff];
-  const int per = meta[kMetaPer];
   TileIter it;
-  if (g >= geff || !it.init(p.ws.ipc, p.B, g, per, p.ws.cta_first[g])) {  // the latter cannot happen for g < geff
+  if (!it.init(p.ws.ipc, p.B, p.ws.cta_desc[2 * g], p.ws.cta_desc[2 * g + 1])) {  // a range beyond the tokens
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     return;
   }
