@@ -406,8 +406,9 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
 // quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
 // pair's bytes are loaded while this pair is converted; one 16-column store per pair).
 // Part 0 finds S_t, hands it to the quarter's other parts through stq and a named
-// barrier, and stores it in tensor-memory column st_col for the softmax group (0 for
-// tokens past the tile).
+// barrier of the quarter's parts (which also orders every part's V^T copy of the
+// previous tile, read from this K buffer, before any part overwrites it), and stores
+// it in tensor-memory column st_col for the softmax group (0 for tokens past the tile).
 __device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
                                                uint32_t st_col, int* stq, uint32_t bar_id) {
   const bool valid = t < n;
@@ -427,7 +428,9 @@ __device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int t0, int n,
       St = (int)max(mhi >> 8, mlo);
     }
     stq[t] = St;
-    named_arrive(bar_id, 32 * kDqParts);
+    // a full barrier, not an arrive: the K buffer this part is about to overwrite held
+    // the previous tile, whose V^T the other parts may still be copying
+    named_sync(bar_id, 32 * kDqParts);
     const uint32_t sv[1] = {(uint32_t)St};
     tmem_st1(st_col, sv);
   } else {
