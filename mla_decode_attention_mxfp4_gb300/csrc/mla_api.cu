@@ -110,7 +110,22 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   const WsOffsets o = ws_offsets(batch, di.grid);
   const mla::Workspace w = ws_bind(ws, o);
   const int kv_null = (kv_packed == nullptr || kv_scale == nullptr) ? 1 : 0;
-  mla::mla_partition_kernel<<<1, 1024, 0, stream>>>(kv_indptr, batch, di.grid, kv_null, w);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    // may be scheduled while the preceding kernel (e.g. the previous call's merge) drains;
+    // it waits for that grid before its first load
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::mla_partition_kernel, kv_indptr, batch, di.grid, kv_null, w) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
   mla::SplitParams sp;
   sp.q = static_cast<const __nv_bfloat16*>(q);
   sp.kv = kv_packed;
@@ -123,9 +138,6 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   // split and merge are launched with programmatic stream serialization: each may be
   // scheduled while its predecessor runs and waits for it with griddepcontrol.wait.  The
   // timed variant records events between the launches, which orders them as usual.
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return MLA_ERR_CUDA;
   {
     cudaLaunchConfig_t cfg = {};

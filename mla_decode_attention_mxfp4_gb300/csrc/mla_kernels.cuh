@@ -245,6 +245,10 @@ __global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __re
   const int tid = threadIdx.x;
   const bool in_smem = B <= kPartSmemSeqs;
   if (tid == 0) s_bad = 0;
+  // Launched with programmatic serialization, this grid may be resident before the
+  // preceding kernel in the stream (the previous call's merge kernel, or whatever wrote
+  // kv_indptr) has finished: wait for it before the first load.
+  grid_dependency_wait();
   __syncthreads();
   const int hi = kv_null ? 0 : max(indptr[B], 0);
   // ipc[i] = clamp(max(indptr[0..i]), 0, indptr[B]); every row index stays below indptr[B]
@@ -961,6 +965,7 @@ constexpr int kMergeThreads = 32 * kHeads;
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws,
                                                                   int B) {
   grid_dependency_wait();  // the split kernel's partials
+  grid_launch_dependents();  // the next call's partition kernel waits for this grid itself
   const int b = blockIdx.x;
   if (b >= B) return;
   const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
