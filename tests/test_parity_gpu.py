@@ -164,6 +164,27 @@ def test_scale_extremes_and_query_range():
         check_close(got[b] / scale, ref[b] / scale, f"extreme[{b}]")
 
 
+def test_running_maxima_move_late_in_a_sequence():
+    """A token far into a sequence whose scale bytes are raised: its scores jump by far
+    more than the raise threshold and so does its token exponent, so the running maxima
+    move in the middle of a segment and the accumulator is rescaled (the full path of the
+    softmax statistics); a later block of tokens with raised exponents does the same for
+    the token-exponent maximum alone."""
+    d = MI.make_custom([1000, 700, 300], seed=71)
+    s = d.kv_scale.clone().to(torch.int32)
+    s[900] += 6                      # one late token 64x larger than the rest
+    s[1000 + 450:1000 + 460] += 9    # a late run of tokens with exponents 9 binades higher
+    s[1700 + 290] -= 20              # a tiny token at the end of the third sequence
+    d.kv_scale = s.clamp(0, 254).to(torch.uint8).contiguous()
+    out, st = gpu_decode(d)
+    assert st == 0
+    ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale)
+    got = as64(out)
+    for b in range(3):  # relative to each sequence's own magnitude
+        scale = np.abs(ref[b]).max()
+        check_close(got[b] / scale, ref[b] / scale, f"late maxima[{b}]")
+
+
 def test_special_cases_zero_query_identical_tokens():
     d = MI.make_custom([77, 40], seed=61)
     q = d.q.clone()
