@@ -117,7 +117,7 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
  *
  * Same arguments, layouts and results as mla_decode_mxfp4.  Instead of a
  * workspace it uses one scratch array that the library defines statically in
- * device memory: about 10.6 MB per GPU that loads the library, held until the
+ * device memory: about 86 MB per GPU that loads the library, held until the
  * process exits, sized for at most 4096 sequences per call and at most 160
  * resident CTAs of the attention kernel (152 on GB300).  Larger requests are
  * rejected with MLA_ERR_WORKSPACE before anything is launched.  It calls no

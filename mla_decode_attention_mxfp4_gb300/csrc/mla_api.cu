@@ -29,7 +29,7 @@ size_t g_ws_bytes[kMaxDevices] = {};
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsOffsets {
-  size_t meta, ipc, seqinfo, cta_desc, lse, acc, total;
+  size_t meta, ipc, seqinfo, cta_desc, lse, acc, qhat, qch, total;
 };
 
 WsOffsets ws_offsets(int batch, int grid) {
@@ -48,6 +48,10 @@ WsOffsets ws_offsets(int batch, int grid) {
   off = align_up(off + slots * mla::kHeads * sizeof(float), 256);
   o.acc = off;
   off = align_up(off + slots * mla::kHeads * mla::kDv * sizeof(float), 256);
+  o.qhat = off;
+  off = align_up(off + (size_t)batch * mla::kQhatBytes, 256);
+  o.qch = off;
+  off = align_up(off + (size_t)batch * mla::kHeads * sizeof(float), 256);
   o.total = off;
   return o;
 }
@@ -61,6 +65,8 @@ mla::Workspace ws_bind(void* base, const WsOffsets& o) {
   w.cta_desc = reinterpret_cast<int4*>(b + o.cta_desc);
   w.part_lse = reinterpret_cast<float*>(b + o.lse);
   w.part_acc = reinterpret_cast<float*>(b + o.acc);
+  w.qhat = b + o.qhat;
+  w.qch = reinterpret_cast<float*>(b + o.qch);
   return w;
 }
 
@@ -117,23 +123,22 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
     // may be scheduled while the preceding kernel (e.g. the previous call's merge) drains;
     // it waits for that grid before its first load
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
+    cfg.gridDim = dim3(1 + (batch + mla::kQhatSeqsPerBlock - 1) / mla::kQhatSeqsPerBlock);
+    cfg.blockDim = dim3(mla::kPartThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, mla::mla_partition_kernel, kv_indptr, batch, di.grid, kv_null, w) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, mla::mla_partition_kernel, kv_indptr, batch, di.grid, kv_null, w,
+                           static_cast<const __nv_bfloat16*>(q), sm_scale) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
   mla::SplitParams sp;
-  sp.q = static_cast<const __nv_bfloat16*>(q);
   sp.kv = kv_packed;
   sp.sc = kv_scale;
   sp.out = static_cast<__nv_bfloat16*>(out);
   sp.ws = w;
   sp.B = batch;
-  sp.sm_scale = sm_scale;
   sp.timeout_ns = 1000000000ull;
   // split and merge are launched with programmatic stream serialization: each may be
   // scheduled while its predecessor runs and waits for it with griddepcontrol.wait.  The
@@ -174,7 +179,9 @@ constexpr size_t kStaticScratchBytes =
     static_align(16 * sizeof(int)) + static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int)) +
     static_align((size_t)kStaticMaxBatch * sizeof(int4)) + static_align(2 * (size_t)kStaticMaxGrid * sizeof(int4)) +
     static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * sizeof(float)) +
-    static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * mla::kDv * sizeof(float));
+    static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * mla::kDv * sizeof(float)) +
+    static_align((size_t)kStaticMaxBatch * mla::kQhatBytes) +
+    static_align((size_t)kStaticMaxBatch * mla::kHeads * sizeof(float));
 
 // One copy per GPU that loads the library, alive until the process exits.
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];

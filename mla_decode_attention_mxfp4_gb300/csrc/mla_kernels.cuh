@@ -9,23 +9,26 @@
 // mla_reduce_v1_like_kernel / 676098 _mla_reduce_kernel), but the partition is
 // built on the device and the per-split arithmetic is organised for GB300:
 //
-//  1. mla_partition_kernel (1 CTA): sanitises kv_indptr, cuts the concatenated
+//  1. mla_partition_kernel: its first CTA sanitises kv_indptr, cuts the concatenated
 //     token stream [indptr[0], indptr[B]) into G equal contiguous ranges (one per
 //     resident CTA), and records, per sequence, which ranges it touches and where
-//     its partial results go.
+//     its partial results go; the other CTAs build each sequence's query operand
+//     (e4m3 hi/lo parts of the prescaled query, in its shared-memory image) and
+//     the per-head score factors.
 //  2. mla_split_kernel (G persistent CTAs, one per SM): each CTA walks its range in
 //     tiles of 128 tokens, one segment per sequence it overlaps.  Warp roles:
 //       warp 0      MMA issue (one elected lane per tcgen05.mma, whole warp
 //                   converged) and the tensor-memory allocation;
-//       warp 1      producer: bulk async copies (packed rows, scale bytes, and the
-//                   query rows at a segment start) into a 3-stage smem ring;
+//       warp 1      producer: bulk async copies (packed rows and scale bytes into a
+//                   3-stage smem ring, the sequence's query operand into one of two
+//                   buffers at a segment start);
 //       warps 2..5  softmax group, one warp per tensor-memory lane quarter (32
 //                   tokens), all 16 heads: online softmax of S^T, P as e4m3 hi + lo
 //                   parts, rescaling of the O^T accumulator, segment epilogue;
 //       warps 6..17 dequant group, three warps per lane quarter: per-token scale
 //                   rebasing, the K tile as e5m2 into tensor memory (A operand of
 //                   QK^T, double-buffered), V^T as e5m2 into shared memory, the
-//                   query operand at a segment start.
+//                   score factors at a segment start.
 //     QK^T (S^T[128 tokens][32] = K . Qhat^T, hi and lo query parts stacked as N)
 //     and P.V (O^T[512][32] += V^T . P^T) run on tcgen05 kind::f8f6f4 with fp32
 //     accumulators in tensor memory.  The groups hand tiles to each other through
@@ -95,13 +98,15 @@ struct Workspace {
   int4* cta_desc;     // [G][2]: range g = {r0, r1, first sequence b, ipc[b]}, {ipc[b+1], -, -, -}
   float* part_lse;    // [2G][16]   log2-sum-exp of each partial
   float* part_acc;    // [2G][16][512] normalised partial output
+  uint8_t* qhat;      // [B][kQhatBytes] query operand of each sequence, in its shared-memory image
+  float* qch;         // [B][16] score factor of each head: sm_scale * log2(e) * 2^E_h
 };
 
 // ---- shared-memory and tensor-memory map of mla_split_kernel ---------------
 constexpr int kStagePackedBytes = kTile * kPacked;                   // 36864
 constexpr int kStageScaleBytes = 2432;                               // >= 128*18 + 32, mult of 16
 constexpr int kStageBytes = kStagePackedBytes + kStageScaleBytes;    // 39296
-constexpr int kQBytes = kHeads * kDqk * 2;                           // 18432 (bf16 Q rows)
+constexpr int kQhatBytes = 32 * kDqk;                                // 18432: e4m3 hi + lo query parts
 
 // Tensor memory (32-bit columns, lane = token of the tile / row of M):
 constexpr uint32_t kTmemCols = 512;
@@ -123,22 +128,20 @@ constexpr uint32_t kPtLbo = 256, kPtSbo = 128, kPtBytes = kTile * 32;
 constexpr int kMaxThresh = 4;  // raise the running maxima only by more than this (log2 units)
 
 constexpr int kOffStages = 0;
-constexpr int kOffQStage = kOffStages + kStages * kStageBytes;            // 117888
-constexpr int kOffQhat = kOffQStage + kQBytes;                            // 136320
-constexpr int kOffVt = kOffQhat + 32 * kDqk;                              // 154752
+constexpr int kOffQhat = kOffStages + kStages * kStageBytes;              // 117888: [2] (segment parity)
+constexpr int kOffVt = kOffQhat + 2 * kQhatBytes;                         // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
 constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][16 heads][4 quarters]
 constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: [2][4] token-exponent maxima
 constexpr int kOffCh = kOffRw + 32;                                       // 229024: [4][16] score factors
-constexpr int kOffEh = kOffCh + 4 * kHeads * 4;                           // 229280
-constexpr int kOffLw = kOffEh + kHeads * 4;                               // 229344: [16 heads][4 quarters]
-constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229600: [16] output factors
-constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229664: [4 warps][16 m, 16 alpha]
-constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230176: [2][128] S_t within a quarter
-constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231200
-constexpr int kOffBar = kOffTmem + 16;                                    // 232240
-constexpr int kNumBars = 14;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 232368
+constexpr int kOffLw = kOffCh + 4 * kHeads * 4;                           // 229280: [16 heads][4 quarters]
+constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229536: [16] output factors
+constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229600: [4 warps][16 m, 16 alpha]
+constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230112: [2][128] S_t within a quarter
+constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136
+constexpr int kOffBar = kOffTmem + 16;                                    // 231152
+constexpr int kNumBars = 15;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231272
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
@@ -148,13 +151,11 @@ constexpr uint32_t kBarDq = 3;     // named barrier of the dequant group
 constexpr uint32_t kBarStq = 4;    // 4 + 4 * (tile parity) + lane quarter: S_t hand-off in a quarter
 
 struct SplitParams {
-  const __nv_bfloat16* q;
   const uint8_t* kv;
   const uint8_t* sc;
   __nv_bfloat16* out;
   Workspace ws;
   int B;
-  float sm_scale;
   unsigned long long timeout_ns;
 };
 
@@ -234,21 +235,102 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_tot, int& t
   return v;
 }
 
-// Sanitise kv_indptr, size the ranges, and describe every sequence's splits.
+// Query operand of one head of one sequence (one warp): per-head prescale exponent E_h,
+// score factor sm_scale * log2(e) * 2^E_h, and the e4m3 hi/lo parts of
+// Qhat = q * 2^-E_h (two e4m3 terms hold a bf16 value exactly unless it lies more than
+// 2^11 below its head's maximum), written as the split kernel's shared-memory image of
+// the operand (offset(n, d) of the Qhat layout; n = h for the hi part, 16 + h for the
+// lo part) so that one bulk copy lands it.  Lane l converts the 16-dim chunks l and
+// l + 32.
+__device__ __forceinline__ void build_qhat_head(const __nv_bfloat16* __restrict__ q, float sm_scale, int b, int h,
+                                                int lane, const Workspace& ws) {
+  const uint4* qr = reinterpret_cast<const uint4*>(q + ((long long)b * kHeads + h) * kDqk);
+  constexpr int kChunks = kDqk / 16;  // 36
+  uint4 x[2][2];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int ch = lane + 32 * c;
+    if (ch < kChunks) {
+      x[c][0] = qr[2 * ch];
+      x[c][1] = qr[2 * ch + 1];
+      const uint32_t w[8] = {x[c][0].x, x[c][0].y, x[c][0].z, x[c][0].w, x[c][1].x, x[c][1].y, x[c][1].z, x[c][1].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  int e = 0;
+  float f = 1.f;
+  if (mx >= 0x7F80u) {
+    f = __int_as_float(0x7FC00000);  // a non-finite query makes the head's scores NaN
+  } else if (mx != 0) {
+    int ex;
+    frexpf(__uint_as_float(mx << 16), &ex);
+    e = ex - 8;  // max |q| * 2^-e in [128, 256): below the e4m3 maximum 448
+  }
+  if (lane == 0) {
+    const int ea = e / 2, eb = e - ea;  // exact 2^e as two factors (e in [-141, 120])
+    ws.qch[b * kHeads + h] = sm_scale * 1.4426950408889634f * exp2i(ea) * exp2i(eb) * f;
+  }
+  const int na = (-e) / 2, nb = -e - na;
+  const float s1 = exp2i(na), s2 = exp2i(nb);
+  uint8_t* img = ws.qhat + (long long)b * kQhatBytes + (h >> 3) * kQSbo + (h & 7) * 16;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int ch = lane + 32 * c;
+    if (ch >= kChunks) continue;
+    const uint32_t w[8] = {x[c][0].x, x[c][0].y, x[c][0].z, x[c][0].w, x[c][1].x, x[c][1].y, x[c][1].z, x[c][1].w};
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      uint32_t hw[2], lw[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float q0 = __uint_as_float(w[i + j] << 16) * s1 * s2;
+        const float q1 = __uint_as_float(w[i + j] & 0xFFFF0000u) * s1 * s2;
+        const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_fp8x2_storage_t lo2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(q0 - hf.x, q1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+        hw[j] = hi2;
+        lw[j] = lo2;
+      }
+      hi[i >> 1] = hw[0] | (hw[1] << 16);
+      lo[i >> 1] = lw[0] | (lw[1] << 16);
+    }
+    *reinterpret_cast<uint4*>(img + ch * kQLbo) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(img + ch * kQLbo + 2 * kQSbo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Block 0: sanitise kv_indptr, size the ranges, and describe every sequence's splits.
 // kv_null: the KV buffers are absent (NULL), so no row may be read.
-__global__ void __launch_bounds__(1024) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
-                                                             int G, int kv_null, Workspace ws) {
+// Blocks 1..: the query operand of sequences 2(x-1) and 2(x-1)+1 (warp w: head w % 16),
+// so the split kernel copies it instead of building it at every segment start.
+constexpr int kPartThreads = 1024;
+constexpr int kQhatSeqsPerBlock = kPartThreads / 32 / kHeads;  // 2
+__global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
+                                                                     int G, int kv_null, Workspace ws,
+                                                                     const __nv_bfloat16* __restrict__ q,
+                                                                     float sm_scale) {
   grid_launch_dependents();  // the split kernel's prologue may run alongside
+  // Launched with programmatic serialization, this grid may be resident before the
+  // preceding kernel in the stream (the previous call's merge kernel, or whatever wrote
+  // kv_indptr or q) has finished: wait for it before the first load.
+  grid_dependency_wait();
+  const int tid = threadIdx.x;
+  if (blockIdx.x > 0) {
+    const int b = (blockIdx.x - 1) * kQhatSeqsPerBlock + (tid >> 5) / kHeads;
+    if (b < B) build_qhat_head(q, sm_scale, b, (tid >> 5) % kHeads, tid & 31, ws);
+    return;
+  }
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_ipc[kPartSmemSeqs + 1];  // copy of ipc for batch <= kPartSmemSeqs
-  const int tid = threadIdx.x;
   const bool in_smem = B <= kPartSmemSeqs;
   if (tid == 0) s_bad = 0;
-  // Launched with programmatic serialization, this grid may be resident before the
-  // preceding kernel in the stream (the previous call's merge kernel, or whatever wrote
-  // kv_indptr) has finished: wait for it before the first load.
-  grid_dependency_wait();
   __syncthreads();
   const int hi = kv_null ? 0 : max(indptr[B], 0);
   // ipc[i] = clamp(max(indptr[0..i]), 0, indptr[B]); every row index stays below indptr[B]
@@ -330,60 +412,6 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, con
   aborted = true;
   atomicOr(&p.ws.meta[kMetaStatus], kDeviceTimeout);
   return false;
-}
-
-// Segment start: per-head prescale exponent, score factor, and the e4m3 hi/lo
-// parts of Qhat = q * 2^-E_h (two e4m3 terms hold a bf16 value exactly unless it
-// lies more than 2^11 below its head's maximum).  Run by the dequant group
-// (gtid 0..383; warp w takes heads w and w + 12); ends with the group's barrier.
-__device__ __forceinline__ void build_qhat(uint8_t* smem, float sm_scale, int chbuf, int gtid, int gwarp, int lane) {
-  const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + kOffQStage);
-  int* eh = reinterpret_cast<int*>(smem + kOffEh);
-  float* ch = reinterpret_cast<float*>(smem + kOffCh) + chbuf * kHeads;
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = gwarp + kDqWarps * hh;
-    if (h >= kHeads) break;
-    const uint16_t* qb = reinterpret_cast<const uint16_t*>(qs) + h * kDqk + lane * 18;
-    uint32_t mx = 0;
-#pragma unroll 6
-    for (int d = 0; d < 18; ++d) mx = max(mx, (uint32_t)(qb[d] & 0x7FFFu));
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0) {
-      int e = 0;
-      float f = 1.f;
-      if (mx >= 0x7F80u) {
-        f = __int_as_float(0x7FC00000);  // a non-finite query makes the head's scores NaN
-      } else if (mx != 0) {
-        int ex;
-        frexpf(__uint_as_float(mx << 16), &ex);
-        e = ex - 8;  // max |q| * 2^-e in [128, 256): below the e4m3 maximum 448
-      }
-      eh[h] = e;
-      const int ea = e / 2, eb = e - ea;  // exact 2^e as two factors (e in [-141, 120])
-      ch[h] = sm_scale * 1.4426950408889634f * exp2i(ea) * exp2i(eb) * f;
-    }
-  }
-  named_sync(kBarDq, kDqThreads);
-  uint8_t* qhat = smem + kOffQhat;
-  for (int e2 = gtid; e2 < kHeads * kDqk / 2; e2 += kDqThreads) {
-    const int h = e2 / (kDqk / 2);
-    const int d = (e2 % (kDqk / 2)) * 2;
-    const int e = eh[h], ea = (-e) / 2, eb = -e - ea;
-    const float s1 = exp2i(ea), s2 = exp2i(eb);
-    const float q0 = __bfloat162float(qs[h * kDqk + d]) * s1 * s2;
-    const float q1 = __bfloat162float(qs[h * kDqk + d + 1]) * s1 * s2;
-    const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3);
-    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
-    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-    const __nv_fp8x2_storage_t lo2 =
-        __nv_cvt_float2_to_fp8x2(make_float2(q0 - hf.x, q1 - hf.y), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t off = (d >> 4) * kQLbo + (h >> 3) * kQSbo + (h & 7) * 16 + (d & 15);
-    *reinterpret_cast<uint16_t*>(qhat + off) = hi2;
-    *reinterpret_cast<uint16_t*>(qhat + off + 2 * kQSbo) = lo2;  // n = 16 + h: two 8-row groups further
-  }
-  fence_proxy_async_smem();  // the tensor cores read Qhat through the async proxy
-  named_sync(kBarDq, kDqThreads);
 }
 
 // f16 2^r as the bit pattern of an f16x2 pair: exponent field r + 15 when normal, a
@@ -510,18 +538,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_full = bars;          // [3] stage landed (producer, tx bytes)
   uint64_t* bar_empty = bars + 3;     // [3] stage consumed (dequant group)
-  uint64_t* bar_qempty = bars + 6;    // query rows consumed (one per segment)
-  uint64_t* bar_kready = bars + 7;    // [2] K tile in tensor-memory buffer b, and its Qhat, ready (dequant group)
-  uint64_t* bar_vready = bars + 9;    // V^T of a tile in shared memory (dequant group)
-  uint64_t* bar_pready = bars + 10;   // P^T and any O^T rescale of a tile done (softmax group)
-  uint64_t* bar_qk = bars + 11;       // [2] S^T buffer b and the tile's S_t written (MMA commit)
-  uint64_t* bar_pv = bars + 13;       // P.V of a tile completed (MMA commit)
+  uint64_t* bar_qfree = bars + 6;     // [2] Qhat buffer b read by the last QK^T of its segment (MMA commit)
+  uint64_t* bar_kready = bars + 8;    // [2] K tile in tensor-memory buffer b ready, its Qhat landed (dequant group)
+  uint64_t* bar_vready = bars + 10;   // V^T of a tile in shared memory (dequant group)
+  uint64_t* bar_pready = bars + 11;   // P^T and any O^T rescale of a tile done (softmax group)
+  uint64_t* bar_qk = bars + 12;       // [2] S^T buffer b and the tile's S_t written (MMA commit)
+  uint64_t* bar_pv = bars + 14;       // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], kDqWarps);
     }
-    mbar_init(bar_qempty, 1);
+    mbar_init(&bar_qfree[0], 1);
+    mbar_init(&bar_qfree[1], 1);
     mbar_init(&bar_kready[0], kDqWarps);
     mbar_init(&bar_kready[1], kDqWarps);
     mbar_init(bar_vready, kDqWarps);
@@ -561,7 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       const int s = k % kStages;
       if (k >= kStages) wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted);
       const int j = it.seg;
-      if (it.first && j >= 1) wait_or_flag(bar_qempty, (j - 1) & 1, p, aborted);
+      // segment j's Qhat goes to buffer j & 1 once the last QK^T of segment j - 2 read it
+      if (it.first && j >= 2) wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted);
       uint8_t* st = smem + kOffStages + s * kStageBytes;
       // scale bytes [18*t0, 18*(t0+n)): 16-byte aligned superset by bulk copy,
       // anything past the last aligned byte of the buffer by plain loads.
@@ -572,12 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       uint8_t* sdst = st + kStagePackedBytes;
       for (long long x = (a1 > a0 ? a1 : a0); x < b1; ++x) sdst[x - a0] = p.sc[x];
       uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > a0 ? (uint32_t)(a1 - a0) : 0u);
-      if (it.first) bytes += kQBytes;
+      if (it.first) bytes += kQhatBytes;
       mbar_arrive_expect_tx(&bar_full[s], bytes);
       bulk_g2s(st, p.kv + (long long)it.t0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
       if (a1 > a0) bulk_g2s(sdst, p.sc + a0, (uint32_t)(a1 - a0), &bar_full[s], pol_kv);
       if (it.first)
-        bulk_g2s(smem + kOffQStage, p.q + (long long)it.b * kHeads * kDqk, kQBytes, &bar_full[s], pol_q);
+        bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
+                 &bar_full[s], pol_q);
       ++k;
     } while (it.next());
     return;
@@ -599,14 +630,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       // QK^T of tile kk (kk = 0 before the loop proper, then kk = k + 1)
       if (kk == 0 || has_next) {
         const int q = kk;
+        const TileIter& qt = kk == 0 ? cur : nxt;
         wait_or_flag(&bar_kready[q & 1], (q >> 1) & 1, p, aborted);
         tc_fence_after();
         const uint32_t bq = q & 1;
+        const uint64_t dq = dq0 + (uint64_t)(((qt.seg & 1) * kQhatBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kDqk / 32; ++ks)
           umma_f8_ts_warp(tmem + kColS + 32 * bq, tmem + kColA + kColsA * bq + 8 * ks,
-                          dq0 + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+                          dq + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
         umma_commit_warp(&bar_qk[bq]);
+        if (qt.last) umma_commit_warp(&bar_qfree[qt.seg & 1]);  // the segment's Qhat buffer may be refilled
       }
       if (kk == 0) continue;
       // P.V of tile k
@@ -648,10 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     const int part = dwarp >> 2;
     const int gtid = tid - kDqWarp0 * 32;  // 0..383
     uint8_t* vt = smem + kOffVt;
+    // Segment j's score factors go to slot j % 4 of the ring, read by the softmax of its
+    // tiles; slot j % 4 was last read by segment j - 4, whose tiles precede tile k - 2 when
+    // segment j starts at tile k + 1, and P.V of tile k - 2 was waited for in iteration k - 1.
+    float* chs = reinterpret_cast<float*>(smem + kOffCh);
     // prologue: tile 0 (a segment start)
+    if (gtid < kHeads) chs[(it.seg & 3) * kHeads + gtid] = p.ws.qch[it.b * kHeads + gtid];
     wait_or_flag(&bar_full[0], 0, p, aborted);
-    build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
-    if (gtid == 0) mbar_arrive(bar_qempty);
     int* stq = reinterpret_cast<int*>(smem + kOffStq);  // [2][128]
     k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, t_lane + kColSt, stq, kBarStq + q4);
     tc_wait_st();
@@ -670,14 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         // for k >= 2 that is implied by the completion of P.V of tile k-2, which the MMA warp issued
         // after QK^T of tile k-1 and which this group waited for in the previous iteration ----
         const int s1 = (k + 1) % kStages;
+        const bool new_seg = it.first && gtid < kHeads;
+        const float chv = new_seg ? p.ws.qch[it.b * kHeads + gtid] : 0.f;
         wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
         if (k == 1) wait_or_flag(&bar_qk[0], 0, p, aborted);
-        if (it.first) {
-          // the next segment's Qhat replaces this one once QK^T of tile k has completed
-          wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
-          build_qhat(smem, p.sm_scale, it.seg & 3, gtid, dwarp, lane);
-          if (gtid == 0) mbar_arrive(bar_qempty);
-        }
+        if (new_seg) chs[(it.seg & 3) * kHeads + gtid] = chv;
         tc_fence_after();
         // S_t of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3, which
         // finished before P.V of tile k-3 (waited for two iterations ago)
