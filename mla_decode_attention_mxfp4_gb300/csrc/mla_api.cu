@@ -29,7 +29,7 @@ size_t g_ws_bytes[kMaxDevices] = {};
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsOffsets {
-  size_t meta, ipc, seqinfo, cta_desc, lse, acc, qhat, qch, total;
+  size_t meta, ipc, cta_desc, lse, acc, qhat, qch, total;
 };
 
 WsOffsets ws_offsets(int batch, int grid) {
@@ -39,8 +39,6 @@ WsOffsets ws_offsets(int batch, int grid) {
   off = align_up(off + 16 * sizeof(int), 256);
   o.ipc = off;
   off = align_up(off + (size_t)(batch + 1) * sizeof(int), 256);
-  o.seqinfo = off;
-  off = align_up(off + (size_t)batch * sizeof(int4), 256);
   o.cta_desc = off;
   off = align_up(off + 2 * (size_t)grid * sizeof(int4), 256);
   const size_t slots = 2 * (size_t)grid;  // split sequences need at most 2 partials per range
@@ -61,7 +59,6 @@ mla::Workspace ws_bind(void* base, const WsOffsets& o) {
   mla::Workspace w;
   w.meta = reinterpret_cast<int*>(b + o.meta);
   w.ipc = reinterpret_cast<int*>(b + o.ipc);
-  w.seqinfo = reinterpret_cast<int4*>(b + o.seqinfo);
   w.cta_desc = reinterpret_cast<int4*>(b + o.cta_desc);
   w.part_lse = reinterpret_cast<float*>(b + o.lse);
   w.part_acc = reinterpret_cast<float*>(b + o.acc);
@@ -177,7 +174,7 @@ constexpr int kStaticMaxGrid = 160;
 constexpr size_t static_align(size_t x) { return (x + 255) / 256 * 256; }
 constexpr size_t kStaticScratchBytes =
     static_align(16 * sizeof(int)) + static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int)) +
-    static_align((size_t)kStaticMaxBatch * sizeof(int4)) + static_align(2 * (size_t)kStaticMaxGrid * sizeof(int4)) +
+    static_align(2 * (size_t)kStaticMaxGrid * sizeof(int4)) +
     static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * sizeof(float)) +
     static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * mla::kDv * sizeof(float)) +
     static_align((size_t)kStaticMaxBatch * mla::kQhatBytes) +

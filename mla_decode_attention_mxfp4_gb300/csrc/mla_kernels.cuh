@@ -89,12 +89,16 @@ constexpr int kDeviceBadIndptr = 1;
 constexpr int kDeviceTimeout = 2;
 
 // meta[] fields written by the partition kernel
-enum MetaField { kMetaN = 0, kMetaPer = 1, kMetaGeff = 2, kMetaStatus = 3, kMetaSlots = 4 };
+enum MetaField { kMetaN = 0, kMetaPer = 1, kMetaGeff = 2, kMetaStatus = 3 };
+
+// Partial slots: range g's first segment writes slot 2g and its last segment slot 2g + 1
+// when they are parts of split sequences (any other segment of a range is a whole
+// sequence).  A sequence b split over ranges f..l therefore has its partials in slots
+// 2f + (b starts after range f's first row), 2(f+1), ..., 2l.
 
 struct Workspace {
   int* meta;          // [16]
   int* ipc;           // [B+1] sanitised indptr
-  int4* seqinfo;      // [B]: first range, last range, partial slot base, -
   int4* cta_desc;     // [G][2]: range g = {r0, r1, first sequence b, ipc[b]}, {ipc[b+1], -, -, -}
   float* part_lse;    // [2G][16]   log2-sum-exp of each partial
   float* part_acc;    // [2G][16][512] normalised partial output
@@ -169,6 +173,7 @@ struct TileIter {
   int r1;      // end of the CTA's range
   int seg;     // segment counter
   bool first, last;
+  bool whole;  // the current segment is its whole sequence
 
   // d0 = {r0, r1, first sequence b, ipc[b]}, d1.x = ipc[b+1] (written by the partition kernel)
   __device__ bool init(const int* ipc_, int B_, int4 d0, int4 d1) {
@@ -184,6 +189,7 @@ struct TileIter {
     seg = 0;
     first = true;
     last = t0 + n >= s1;
+    whole = d0.w >= r0 && d1.x <= r1;
     return n > 0;
   }
   __device__ bool next() {
@@ -200,6 +206,7 @@ struct TileIter {
     if (b >= B || ipc[b] >= r1) return false;
     t0 = ipc[b];
     s1 = min(r1, ipc[b + 1]);
+    whole = ipc[b + 1] <= r1;
     n = min(kTile, s1 - t0);
     ++seg;
     first = true;
@@ -358,25 +365,6 @@ __global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32
   const long long per_ll = max((long long)kMinPerCta, ((long long)N + G - 1) / G);
   const int per = (int)per_ll;
   const int geff = N > 0 ? (int)(((long long)N + per - 1) / per) : 0;
-  // per sequence: ranges [f, l] it overlaps; slot base for split sequences
-  int run = 0;
-  for (int base = 0; base < B; base += 1024) {
-    const int b = base + tid;
-    int f = 0, l = -1, nsplit = 0;
-    if (b < B) {
-      const int a0 = ipc[b], a1 = ipc[b + 1];
-      if (a1 > a0) {
-        f = (a0 - rbase) / per;
-        l = (a1 - 1 - rbase) / per;
-        nsplit = l - f + 1;
-      }
-    }
-    const int contrib = nsplit >= 2 ? nsplit : 0;
-    int tot;
-    const int incl = block_inclusive_scan<false>(contrib, warp_tot, tot);
-    if (b < B) ws.seqinfo[b] = make_int4(f, l, run + incl - contrib, 0);
-    run += tot;
-  }
   // per range: its rows, its first sequence (largest b with ipc[b] <= r0) and that
   // sequence's rows, so a CTA starts from one 32-byte load; empty ranges have r0 == r1
   for (int g = tid; g < G; g += 1024) {
@@ -400,7 +388,6 @@ __global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32
     ws.meta[kMetaPer] = per;
     ws.meta[kMetaGeff] = geff;
     ws.meta[kMetaStatus] = s_bad ? kDeviceBadIndptr : 0;
-    ws.meta[kMetaSlots] = run;
   }
 }
 
@@ -941,9 +928,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         const float ls = warp_reduce16<false>(l_part, lane);
         if ((lane & 1) == 0) lw[(lane >> 1) * 4 + q4] = ls;
         named_sync(kBarSm, kSmThreads);
-        const int4 si = p.ws.seqinfo[it.b];
-        const bool whole = si.x == si.y;
-        const int slot = si.z + (g - si.x);
+        const bool whole = it.whole;
+        const int slot = 2 * g + (it.seg > 0 ? 1 : 0);
         if (stid < kHeads) {
           const int h = stid;
           const float4 l4 = *reinterpret_cast<const float4*>(lw + h * 4);
@@ -998,77 +984,102 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 constexpr int kMergeThreads = 32 * kHeads;
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws,
                                                                   int B) {
-  grid_dependency_wait();  // the split kernel's partials
-  grid_launch_dependents();  // the next call's partition kernel waits for this grid itself
+  // The partition written by the partition kernel (complete before the split kernel, this
+  // grid's predecessor, started) is read while the split kernel drains; its partials only
+  // after griddepcontrol.wait.
   const int b = blockIdx.x;
   if (b >= B) return;
   const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
-  const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1];
+  const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1], rbase = ws.ipc[0], per = ws.meta[kMetaPer];
   uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
-  if (a1 <= a0) {  // empty sequence -> zeros
+  if (a1 <= a0) {  // empty sequence -> zeros (the split kernel writes no row of it)
     dst[0] = make_uint4(0, 0, 0, 0);
     dst[1] = make_uint4(0, 0, 0, 0);
     return;
   }
-  const int4 si = ws.seqinfo[b];
-  const int ns = si.y - si.x + 1;
-  if (ns < 2) return;  // written by the split kernel
-  const int base = si.z;
-  // the first two partials' rows are requested together with the weights (one round trip
-  // to L2 for the common two-way split)
-  const float4* p0 = reinterpret_cast<const float4*>(ws.part_acc + ((long long)base * kHeads + h) * kDv + lane * 16);
-  const float4* p1 = p0 + kHeads * kDv / 4;
-  float4 y0[4], y1[4];
+  const int f = (a0 - rbase) / per, l = (a1 - 1 - rbase) / per;
+  const int ns = l - f + 1;
+  if (ns < 2) return;  // a whole sequence: written by the split kernel
+  // partial i of this sequence is in slot 2(f + i), the first one shifted by one when the
+  // sequence is not the first of range f
+  const int shift0 = a0 != rbase + f * per ? 1 : 0;
+  auto slot_of = [&](int i) { return 2 * (f + i) + (i == 0 ? shift0 : 0); };
+  grid_dependency_wait();  // the split kernel's partials
+  grid_launch_dependents();  // the next call's partition kernel waits for this grid itself
+  // the rows of up to kPre partials are requested together with the weights (one round
+  // trip to memory for splits of up to kPre ways)
+  constexpr int kPre = 4;
+  auto row = [&](int i) {
+    return reinterpret_cast<const float4*>(ws.part_acc + ((long long)slot_of(i) * kHeads + h) * kDv + lane * 16);
+  };
+  float4 y[kPre][4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    y0[q] = p0[q];
-    y1[q] = ns > 1 ? p1[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < kPre; ++j) {
+    const float4* pj = row(j < ns ? j : 0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) y[j][q] = j < ns ? pj[q] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   // lane i holds the weight of partials i, i+32, ...; M over all partials first
   float M = -INFINITY;
-  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ws.part_lse[(base + i) * kHeads + h]);
+  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ws.part_lse[slot_of(i) * kHeads + h]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  auto add2 = [&](float w0, const float4 (&x0)[4], float w1, const float4 (&x1)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[4 * q] += w0 * x0[q].x + w1 * x1[q].x;
+      acc[4 * q + 1] += w0 * x0[q].y + w1 * x1[q].y;
+      acc[4 * q + 2] += w0 * x0[q].z + w1 * x1[q].z;
+      acc[4 * q + 3] += w0 * x0[q].w + w1 * x1[q].w;
+    }
+  };
+  auto add1 = [&](float w0, const float4 (&x0)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[4 * q] += w0 * x0[q].x;
+      acc[4 * q + 1] += w0 * x0[q].y;
+      acc[4 * q + 2] += w0 * x0[q].z;
+      acc[4 * q + 3] += w0 * x0[q].w;
+    }
+  };
   float L = 0.f;
   for (int c0 = 0; c0 < ns; c0 += 32) {
     const int cn = min(32, ns - c0);
-    const float wl = lane < cn ? ex2(ws.part_lse[(base + c0 + lane) * kHeads + h] - M) : 0.f;
+    const float wl = lane < cn ? ex2(ws.part_lse[slot_of(c0 + lane) * kHeads + h] - M) : 0.f;
     L += wl;
     int i = 0;
+    if (c0 == 0) {  // the preloaded partials, in pairs (static indices into y)
+#pragma unroll
+      for (int pr = 0; pr < kPre; pr += 2) {
+        if (i == pr && pr + 1 < cn) {
+          add2(__shfl_sync(0xffffffffu, wl, pr), y[pr], __shfl_sync(0xffffffffu, wl, pr + 1), y[pr + 1]);
+          i = pr + 2;
+        } else if (i == pr && pr < cn) {
+          add1(__shfl_sync(0xffffffffu, wl, pr), y[pr]);
+          i = pr + 1;
+        }
+      }
+    }
     for (; i + 1 < cn; i += 2) {  // two partials' loads in flight
-      const float w0 = __shfl_sync(0xffffffffu, wl, i), w1 = __shfl_sync(0xffffffffu, wl, i + 1);
-      const float4* s0 =
-          reinterpret_cast<const float4*>(ws.part_acc + ((long long)(base + c0 + i) * kHeads + h) * kDv + lane * 16);
-      const float4* s1 = s0 + kHeads * kDv / 4;
+      const float4* s0 = row(c0 + i);
+      const float4* s1 = row(c0 + i + 1);
       float4 x0[4], x1[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        x0[q] = c0 + i == 0 ? y0[q] : s0[q];
-        x1[q] = c0 + i == 0 ? y1[q] : s1[q];
+        x0[q] = s0[q];
+        x1[q] = s1[q];
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[4 * q] += w0 * x0[q].x + w1 * x1[q].x;
-        acc[4 * q + 1] += w0 * x0[q].y + w1 * x1[q].y;
-        acc[4 * q + 2] += w0 * x0[q].z + w1 * x1[q].z;
-        acc[4 * q + 3] += w0 * x0[q].w + w1 * x1[q].w;
-      }
+      add2(__shfl_sync(0xffffffffu, wl, i), x0, __shfl_sync(0xffffffffu, wl, i + 1), x1);
     }
     if (i < cn) {
-      const float w0 = __shfl_sync(0xffffffffu, wl, i);
-      const float4* s0 =
-          reinterpret_cast<const float4*>(ws.part_acc + ((long long)(base + c0 + i) * kHeads + h) * kDv + lane * 16);
+      const float4* s0 = row(c0 + i);
+      float4 x0[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 x = s0[q];
-        acc[4 * q] += w0 * x.x;
-        acc[4 * q + 1] += w0 * x.y;
-        acc[4 * q + 2] += w0 * x.z;
-        acc[4 * q + 3] += w0 * x.w;
-      }
+      for (int q = 0; q < 4; ++q) x0[q] = s0[q];
+      add1(__shfl_sync(0xffffffffu, wl, i), x0);
     }
   }
 #pragma unroll

@@ -4,7 +4,9 @@ Re-derives, in Python, what mla_partition_kernel and mla_split_kernel's tile
 iterator compute, and checks the invariants every launch relies on: every
 token row is visited exactly once, all reads stay inside [0, kv_indptr[batch])
 rows and inside the caller's scale bytes, every smem copy fits its stage, and
-partial slots are unique and below the workspace bound of 2 slots per CTA.
+partial slots (range g's first segment -> slot 2g, its last -> 2g + 1) are
+unique, below the workspace bound of 2 slots per CTA, and exactly the slots
+the merge kernel derives for each split sequence from kv_indptr alone.
 """
 import random
 
@@ -26,21 +28,23 @@ def partition(indptr, G, kv_null=False):
     N = ipc[B] - ipc[0]
     per = max(MIN_PER, -(-N // G))
     geff = -(-N // per) if N > 0 else 0
-    seqinfo, run = [], 0
-    for b in range(B):
-        a0, a1 = ipc[b], ipc[b + 1]
-        if a1 > a0:
-            f, l = (a0 - ipc[0]) // per, (a1 - 1 - ipc[0]) // per
-        else:
-            f, l = 0, -1
-        ns = l - f + 1
-        seqinfo.append((f, l, run))
-        run += ns if ns >= 2 else 0
     cta_first = []
     for g in range(geff):
         r0 = ipc[0] + g * per
         cta_first.append(max(b for b in range(B) if ipc[b] <= r0))
-    return ipc, per, geff, seqinfo, run, cta_first, bad
+    return ipc, per, geff, cta_first, bad
+
+
+def merge_slots(ipc, per, b):
+    """Slots the merge kernel reads for sequence b (None: whole or empty sequence)."""
+    a0, a1, rbase = ipc[b], ipc[b + 1], ipc[0]
+    if a1 <= a0:
+        return None
+    f, l = (a0 - rbase) // per, (a1 - 1 - rbase) // per
+    if f == l:
+        return None
+    shift0 = 1 if a0 != rbase + f * per else 0
+    return [2 * (f + i) + (shift0 if i == 0 else 0) for i in range(l - f + 1)]
 
 
 def tiles(ipc, B, g, per, first_seq):
@@ -71,17 +75,20 @@ def tiles(ipc, B, g, per, first_seq):
 
 def check(indptr, G=152, kv_null=False):
     B = len(indptr) - 1
-    ipc, per, geff, seqinfo, slots, cta_first, bad = partition(indptr, G, kv_null)
+    ipc, per, geff, cta_first, bad = partition(indptr, G, kv_null)
     rows_limit = 0 if kv_null else max(indptr[B], 0)  # caller guarantees indptr[batch] rows
     assert all(ipc[i] <= ipc[i + 1] for i in range(B))
-    assert geff <= G and slots <= 2 * G
+    assert geff <= G
     seen = set()
     used_slots = set()
+    slots_of = {}
     scale_end = ipc[B] * NSCALE
     for g in range(geff):
         tl = tiles(ipc, B, g, per, cta_first[g])
         assert tl, g
         for (b, seg, t0, n, first, last) in tl:
+            if first:
+                seg_start = t0
             assert 0 <= ipc[b] <= t0 and t0 + n <= ipc[b + 1] <= rows_limit
             assert 1 <= n <= TILE
             for r in range(t0, t0 + n):
@@ -95,16 +102,15 @@ def check(indptr, G=152, kv_null=False):
                 assert a1 <= scale_end and (a1 - a0) % 16 == 0 and a0 % 16 == 0
             assert b1 - a0 <= STAGE_SCALE_BYTES
             if last:
-                f, l, base = seqinfo[b]
-                if f != l:
-                    slot = base + (g - f)
+                whole = seg_start == ipc[b] and t0 + n == ipc[b + 1]
+                if not whole:
+                    slot = 2 * g + (1 if seg > 0 else 0)
                     assert slot not in used_slots and 0 <= slot < 2 * G
                     used_slots.add(slot)
+                    slots_of.setdefault(b, []).append(slot)
     assert sorted(seen) == list(range(ipc[0], ipc[B]))
     for b in range(B):
-        f, l, base = seqinfo[b]
-        if l > f:
-            assert all(base + i in used_slots for i in range(l - f + 1))
+        assert merge_slots(ipc, per, b) == slots_of.get(b), b
     return bad
 
 
