@@ -988,24 +988,27 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16*
   // grid's predecessor, started) is read while the split kernel drains; its partials only
   // after griddepcontrol.wait.
   const int b = blockIdx.x;
-  if (b >= B) return;
   const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
   const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1], rbase = ws.ipc[0], per = ws.meta[kMetaPer];
   uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
+  int f = 0, ns = 0;
   if (a1 <= a0) {  // empty sequence -> zeros (the split kernel writes no row of it)
     dst[0] = make_uint4(0, 0, 0, 0);
     dst[1] = make_uint4(0, 0, 0, 0);
-    return;
+  } else {
+    f = (a0 - rbase) / per;
+    ns = (a1 - 1 - rbase) / per - f + 1;  // ns == 1: a whole sequence, written by the split kernel
   }
-  const int f = (a0 - rbase) / per, l = (a1 - 1 - rbase) / per;
-  const int ns = l - f + 1;
-  if (ns < 2) return;  // a whole sequence: written by the split kernel
+  // Every CTA waits for the split grid, also those with nothing to merge: this grid must not
+  // complete before its predecessor, since the next kernel in the stream (launched
+  // programmatically) may start as soon as it does and rewrites the workspace.
+  grid_dependency_wait();  // the split kernel's partials
+  grid_launch_dependents();  // the next call's partition kernel waits for this grid itself
+  if (ns < 2) return;
   // partial i of this sequence is in slot 2(f + i), the first one shifted by one when the
   // sequence is not the first of range f
   const int shift0 = a0 != rbase + f * per ? 1 : 0;
   auto slot_of = [&](int i) { return 2 * (f + i) + (i == 0 ? shift0 : 0); };
-  grid_dependency_wait();  // the split kernel's partials
-  grid_launch_dependents();  // the next call's partition kernel waits for this grid itself
   // the rows of up to kPre partials are requested together with the weights (one round
   // trip to memory for splits of up to kPre ways)
   constexpr int kPre = 4;

@@ -111,6 +111,7 @@ def test_kv_len_one_reproduces_v_exactly():
     [127, 128, 129, 255, 256, 257],
     [0, 3, 0, 0, 1, 2, 0],
     [50000],
+    [9000, 20000, 3000, 0, 12000, 1, 7000],
     [0, 0],
     [5] * 300,
 ])
