@@ -95,12 +95,12 @@ int device_info(int dev, DeviceInfo* out) {
 
 int check_args(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, const int32_t* kv_indptr,
                const void* out, int batch, float sm_scale) {
-  (void)kv_scale;
   if (batch < 0) return MLA_ERR_BAD_BATCH;
   if (batch == 0) return MLA_OK;
   if (!q || !kv_indptr || !out) return MLA_ERR_NULL_PTR;
+  // bulk async copies of the scale bytes start on 16-byte boundaries of kv_scale
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv_packed) |
-       reinterpret_cast<uintptr_t>(out)) & 15u)
+       reinterpret_cast<uintptr_t>(kv_scale) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return MLA_ERR_BAD_ALIGN;
   if (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) return MLA_ERR_BAD_ALIGN;
   if (!std::isfinite(sm_scale)) return MLA_ERR_BAD_SCALE;
@@ -154,7 +154,7 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return MLA_ERR_CUDA;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(batch);
+    cfg.gridDim = dim3(batch, mla::kHeads / mla::kMergeHeads);
     cfg.blockDim = dim3(mla::kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -979,16 +979,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 }
 
 // ---- merge of split sequences -------------------------------------------------------
-// One CTA per sequence, warp h = head h, lane l = dims 16l..16l+15:
+// CTA (b, y) merges heads 4y..4y+3 of sequence b (four CTAs per sequence spread the partial
+// loads over more SMs), warp w = head 4y + w, lane l = dims 16l..16l+15:
 // out = sum_s 2^(lse_s - M) acc_s / sum_s 2^(lse_s - M), M = max_s lse_s; empty -> zeros.
-constexpr int kMergeThreads = 32 * kHeads;
+constexpr int kMergeHeads = 4;  // heads per CTA: kHeads / kMergeHeads CTAs per sequence
+constexpr int kMergeThreads = 32 * kMergeHeads;
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16* __restrict__ out, Workspace ws,
                                                                   int B) {
   // The partition written by the partition kernel (complete before the split kernel, this
   // grid's predecessor, started) is read while the split kernel drains; its partials only
   // after griddepcontrol.wait.
   const int b = blockIdx.x;
-  const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, h = (tid >> 5) + kMergeHeads * blockIdx.y, lane = tid & 31;
   const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1], rbase = ws.ipc[0], per = ws.meta[kMetaPer];
   uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
   int f = 0, ns = 0;
