@@ -22,9 +22,9 @@
  *   kv_scale   uint8 [rows][18]         E8M0; byte 0xFF is NaN, byte 0 is 2^-127
  *   kv_indptr  int32 [batch+1]          device memory; rows used are [kv_indptr[0], kv_indptr[batch])
  *   out        bf16  [batch][16][512]   written for every b (an empty sequence gives zeros)
- * Buffers must hold at least kv_indptr[batch] rows.  q, kv_packed, kv_scale and out
- * must be 16-byte aligned (the scale rows themselves are 18 bytes apart), kv_indptr
- * 4-byte aligned.
+ * Buffers must hold at least kv_indptr[batch] rows.  q, kv_packed and out must be
+ * 16-byte aligned, kv_indptr 4-byte aligned; kv_scale has no alignment rule (bytes
+ * before its first and after its last 16-byte boundary are read with plain loads).
  * out must not alias any input.  kv_packed and kv_scale may be NULL when there are
  * no KV rows; the device then treats every sequence as empty (zero output) and
  * flags MLA_DEVICE_BAD_INDPTR if kv_indptr claims rows.

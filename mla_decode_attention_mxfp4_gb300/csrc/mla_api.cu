@@ -98,9 +98,8 @@ int check_args(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
   if (batch < 0) return MLA_ERR_BAD_BATCH;
   if (batch == 0) return MLA_OK;
   if (!q || !kv_indptr || !out) return MLA_ERR_NULL_PTR;
-  // bulk async copies of the scale bytes start on 16-byte boundaries of kv_scale
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv_packed) |
-       reinterpret_cast<uintptr_t>(kv_scale) | reinterpret_cast<uintptr_t>(out)) & 15u)
+       reinterpret_cast<uintptr_t>(out)) & 15u)
     return MLA_ERR_BAD_ALIGN;
   if (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) return MLA_ERR_BAD_ALIGN;
   if (!std::isfinite(sm_scale)) return MLA_ERR_BAD_SCALE;
@@ -132,7 +131,9 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   }
   mla::SplitParams sp;
   sp.kv = kv_packed;
-  sp.sc = kv_scale;
+  // kv_scale has no alignment rule: the kernel addresses it from the 16-byte boundary below it
+  sp.sc_mis = (int)(reinterpret_cast<uintptr_t>(kv_scale) & 15u);
+  sp.sc = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(kv_scale) - (uintptr_t)sp.sc_mis);
   sp.out = static_cast<__nv_bfloat16*>(out);
   sp.ws = w;
   sp.B = batch;

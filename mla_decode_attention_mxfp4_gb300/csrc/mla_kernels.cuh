@@ -156,7 +156,8 @@ constexpr uint32_t kBarStq = 4;    // 4 + 4 * (tile parity) + lane quarter: S_t 
 
 struct SplitParams {
   const uint8_t* kv;
-  const uint8_t* sc;
+  const uint8_t* sc;  // the 16-byte boundary at or below kv_scale (kv_scale = sc + sc_mis)
+  int sc_mis;         // kv_scale's offset from that boundary (0..15)
   __nv_bfloat16* out;
   Workspace ws;
   int B;
@@ -429,22 +430,29 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
 // previous tile, read from this K buffer, before any part overwrites it), and stores
 // it in tensor-memory column st_col for the softmax group (0 for tokens past the tile).
 __device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
-                                               uint32_t st_col, int* stq, uint32_t bar_id) {
+                                               uint32_t st_col, int* stq, uint32_t bar_id, int sc_mis) {
   const bool valid = t < n;
-  const uint8_t* sb = st + kStagePackedBytes + (int)(((long long)t0 * kNScale) & 15) + t * kNScale;
+  const uint8_t* sb = st + kStagePackedBytes + (int)((sc_mis + (long long)t0 * kNScale) & 15) + t * kNScale;
   int St = 0;
   if (part == 0) {
     if (valid) {
-      // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
-      // high byte of the largest 16-bit word
-      uint32_t mhi = 0, mlo = 0;
+      if ((smem_u32(sb) & 1u) == 0) {
+        // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
+        // high byte of the largest 16-bit word
+        uint32_t mhi = 0, mlo = 0;
 #pragma unroll
-      for (int i = 0; i < kNScale / 2; ++i) {
-        const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
-        mhi = max(mhi, two);
-        mlo = max(mlo, two & 0xFFu);
+        for (int i = 0; i < kNScale / 2; ++i) {
+          const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
+          mhi = max(mhi, two);
+          mlo = max(mlo, two & 0xFFu);
+        }
+        St = (int)max(mhi >> 8, mlo);
+      } else {  // odd address (kv_scale at an odd offset from a 16-byte boundary): byte loads
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < kNScale; ++i) m = max(m, (uint32_t)sb[i]);
+        St = (int)m;
       }
-      St = (int)max(mhi >> 8, mlo);
     }
     stq[t] = St;
     // a full barrier, not an arrive: the K buffer this part is about to overwrite held
@@ -570,8 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    const long long scale_end = (long long)p.ws.ipc[p.B] * kNScale;  // bytes of kv_scale in use
+    // scale byte x of token row r is at sc[sc_mis + 18r]; the bytes in use end at scale_end, and
+    // the buffer's first 16-byte boundary is head16
+    const long long scale_end = p.sc_mis + (long long)p.ws.ipc[p.B] * kNScale;
     const long long scale_end16 = scale_end & ~15LL;
+    const long long head16 = (p.sc_mis + 15) & ~15LL;
     int k = 0;
     do {
       const int s = k % kStages;
@@ -580,19 +591,22 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       // segment j's Qhat goes to buffer j & 1 once the last QK^T of segment j - 2 read it
       if (it.first && j >= 2) wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted);
       uint8_t* st = smem + kOffStages + s * kStageBytes;
-      // scale bytes [18*t0, 18*(t0+n)): 16-byte aligned superset by bulk copy,
-      // anything past the last aligned byte of the buffer by plain loads.
-      const long long b0 = (long long)it.t0 * kNScale, b1 = (long long)(it.t0 + it.n) * kNScale;
+      // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
+      // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
+      // buffer's first boundary and past its last one by plain loads
+      const long long b0 = p.sc_mis + (long long)it.t0 * kNScale, b1 = p.sc_mis + (long long)(it.t0 + it.n) * kNScale;
       const long long a0 = b0 & ~15LL;
+      const long long c0 = a0 > head16 ? a0 : head16;
       long long a1 = (b1 + 15) & ~15LL;
       if (a1 > scale_end16) a1 = scale_end16;
       uint8_t* sdst = st + kStagePackedBytes;
-      for (long long x = (a1 > a0 ? a1 : a0); x < b1; ++x) sdst[x - a0] = p.sc[x];
-      uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > a0 ? (uint32_t)(a1 - a0) : 0u);
+      for (long long x = b0; x < b1 && x < c0; ++x) sdst[x - a0] = p.sc[x];
+      for (long long x = (a1 > c0 ? a1 : c0); x < b1; ++x) sdst[x - a0] = p.sc[x];
+      uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > c0 ? (uint32_t)(a1 - c0) : 0u);
       if (it.first) bytes += kQhatBytes;
       mbar_arrive_expect_tx(&bar_full[s], bytes);
       bulk_g2s(st, p.kv + (long long)it.t0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
-      if (a1 > a0) bulk_g2s(sdst, p.sc + a0, (uint32_t)(a1 - a0), &bar_full[s], pol_kv);
+      if (a1 > c0) bulk_g2s(sdst + (c0 - a0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
       if (it.first)
         bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
                  &bar_full[s], pol_q);
@@ -677,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     if (gtid < kHeads) chs[(it.seg & 3) * kHeads + gtid] = p.ws.qch[it.b * kHeads + gtid];
     wait_or_flag(&bar_full[0], 0, p, aborted);
     int* stq = reinterpret_cast<int*>(smem + kOffStq);  // [2][128]
-    k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, t_lane + kColSt, stq, kBarStq + q4);
+    k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, t_lane + kColSt, stq, kBarStq + q4,
+                   p.sc_mis);
     tc_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -704,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         // finished before P.V of tile k-3 (waited for two iterations ago)
         k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.t0, it.n, t, part,
                        t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
-                       stq + ((k + 1) & 1) * kTile, kBarStq + 4 * ((k + 1) & 1) + q4);
+                       stq + ((k + 1) & 1) * kTile, kBarStq + 4 * ((k + 1) & 1) + q4, p.sc_mis);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();

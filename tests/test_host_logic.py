@@ -73,7 +73,21 @@ def tiles(ipc, B, g, per, first_seq):
         t0, s1, seg, first = ipc[b], min(r1, ipc[b + 1]), seg + 1, True
 
 
-def check(indptr, G=152, kv_null=False):
+def scale_copy_plan(t0, n, mis, scale_end):
+    """The producer's plan for a tile's scale bytes, offsets from the 16-byte boundary at or
+    below kv_scale (kv_scale itself at offset mis): (a0, plain byte offsets, bulk range)."""
+    b0, b1 = mis + t0 * NSCALE, mis + (t0 + n) * NSCALE
+    a0 = b0 & ~15
+    head16 = (mis + 15) & ~15
+    c0 = max(a0, head16)
+    a1 = min((b1 + 15) & ~15, scale_end & ~15)
+    plain = [(b0, min(b1, c0)), (max(a1, c0), b1)]  # [lo, hi) intervals, possibly empty
+    plain = [(lo, hi) for lo, hi in plain if hi > lo]
+    bulk = (c0, a1) if a1 > c0 else None
+    return b0, b1, a0, plain, bulk
+
+
+def check(indptr, G=152, kv_null=False, mis=0):
     B = len(indptr) - 1
     ipc, per, geff, cta_first, bad = partition(indptr, G, kv_null)
     rows_limit = 0 if kv_null else max(indptr[B], 0)  # caller guarantees indptr[batch] rows
@@ -82,7 +96,7 @@ def check(indptr, G=152, kv_null=False):
     seen = set()
     used_slots = set()
     slots_of = {}
-    scale_end = ipc[B] * NSCALE
+    scale_end = mis + ipc[B] * NSCALE  # the buffer is [mis, mis + 18 * rows) from the boundary below it
     for g in range(geff):
         tl = tiles(ipc, B, g, per, cta_first[g])
         assert tl, g
@@ -94,13 +108,19 @@ def check(indptr, G=152, kv_null=False):
             for r in range(t0, t0 + n):
                 assert r not in seen
                 seen.add(r)
-            # scale bytes: aligned superset by bulk copy, clamped, tail by plain loads
-            b0, b1 = t0 * NSCALE, (t0 + n) * NSCALE
-            a0 = b0 & ~15
-            a1 = min((b1 + 15) & ~15, scale_end & ~15)
-            if a1 > a0:
-                assert a1 <= scale_end and (a1 - a0) % 16 == 0 and a0 % 16 == 0
-            assert b1 - a0 <= STAGE_SCALE_BYTES
+            # scale bytes: 16-byte chunks inside the buffer by bulk copy, the rest by plain
+            # loads; together exactly the tile's bytes, never a byte outside the buffer
+            b0, b1, a0, plain, bulk = scale_copy_plan(t0, n, mis, scale_end)
+            pieces = list(plain)
+            if bulk:
+                c0, a1 = bulk
+                assert c0 % 16 == 0 and a1 % 16 == 0 and mis <= c0 < a1 <= scale_end
+                pieces.append(bulk)
+            assert all(mis <= lo and hi <= scale_end and hi - lo <= 16 for lo, hi in plain)
+            pieces.sort()
+            assert pieces[0][0] <= b0 and pieces[-1][1] >= b1  # no gap inside [b0, b1):
+            assert all(pieces[i][1] >= pieces[i + 1][0] for i in range(len(pieces) - 1))
+            assert all(lo - a0 >= 0 and hi - a0 <= STAGE_SCALE_BYTES for lo, hi in pieces)
             if last:
                 whole = seg_start == ipc[b] and t0 + n == ipc[b + 1]
                 if not whole:
@@ -129,8 +149,8 @@ def test_partition_covers_every_row_once(G):
         for x in lens:
             ip.append(ip[-1] + x)
         cases.append(ip)
-    for ip in cases:
-        assert not check(ip, G)
+    for i, ip in enumerate(cases):
+        assert not check(ip, G, mis=(0, 1, 7, 15)[i % 4])
 
 
 def test_ragged_workload_partition():

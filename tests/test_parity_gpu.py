@@ -223,6 +223,30 @@ def test_workspace_stream_and_determinism():
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
+@pytest.mark.parametrize("offset", [1, 7, 13])
+def test_scale_buffer_off_a_16_byte_boundary(offset):
+    """kv_scale has no alignment rule: a view starting `offset` bytes past a 16-byte
+    boundary gives the same bits as the aligned buffer (the producer loads the bytes
+    before the buffer's first boundary and after its last one with plain loads)."""
+    from mla_decode_attention_mxfp4_gb300 import decode, device_status
+    d = MI.make_custom([300, 129, 0, 1000, 5], seed=90 + offset)
+    dev = torch.device("cuda:0")
+    q, kv, ip = d.q.to(dev), d.kv_packed.to(dev), d.kv_indptr.to(dev)
+    sc = d.kv_scale.to(dev).contiguous()
+    raw = torch.empty(sc.numel() + 32, dtype=torch.uint8, device=dev)
+    shifted = raw[offset:offset + sc.numel()].view(sc.shape)
+    shifted.copy_(sc)
+    assert shifted.data_ptr() % 16 == offset
+    torch.cuda.synchronize()
+    a = decode(q, kv, sc, ip, d.sm_scale)
+    b = decode(q, kv, shifted, ip, d.sm_scale)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.equal(a, b)
+    ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale)
+    check_close(as64(b), ref, f"scale offset {offset}")
+
+
 def test_malformed_indptr_is_flagged_and_in_bounds():
     d = MI.make_custom([30, 30], seed=81)
     d.kv_indptr = torch.tensor([0, 50, 20], dtype=torch.int32)  # decreasing: clamped to rows < 20
