@@ -139,6 +139,11 @@ int mla_decode_mxfp4_noalloc(const void* q, const uint8_t* kv_packed, const uint
  * of the current device).  Returns MLA_OK or MLA_ERR_CUDA. */
 int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, int* status);
 
+/* Same for the library workspace of the current device: the status of the last
+ * mla_decode_mxfp4 call (equivalent to mla_decode_mxfp4_device_status(stream, NULL,
+ * status)). */
+int mla_decode_mxfp4_last_device_status(mla_stream_t stream, int* status);
+
 /* Free the library-owned workspaces of every device (synchronises each device
  * that had one).  Safe to call at any time when no call is in flight. */
 void mla_decode_mxfp4_release(void);

@@ -63,6 +63,8 @@ def lib():
     L.mla_decode_mxfp4_workspace_bytes.argtypes = [i, i]
     L.mla_decode_mxfp4_device_status.restype = i
     L.mla_decode_mxfp4_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    L.mla_decode_mxfp4_last_device_status.restype = i
+    L.mla_decode_mxfp4_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     L.mla_decode_mxfp4_release.restype = None
     L.mla_decode_mxfp4_release.argtypes = []
     L.mla_status_string.restype = ctypes.c_char_p
@@ -111,6 +113,14 @@ def mla_decode_mxfp4_device_status(stream=None, workspace=None) -> int:
     rc = lib().mla_decode_mxfp4_device_status(stream, workspace, ctypes.byref(st))
     if rc != MLA_OK:
         raise MlaError(rc, "mla_decode_mxfp4_device_status")
+    return st.value
+
+
+def mla_decode_mxfp4_last_device_status(stream=None) -> int:
+    st = ctypes.c_int(0)
+    rc = lib().mla_decode_mxfp4_last_device_status(stream, ctypes.byref(st))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_decode_mxfp4_last_device_status")
     return st.value
 
 

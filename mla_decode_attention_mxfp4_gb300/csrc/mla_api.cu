@@ -311,6 +311,10 @@ int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, i
   return MLA_OK;
 }
 
+int mla_decode_mxfp4_last_device_status(mla_stream_t stream, int* status) {
+  return mla_decode_mxfp4_device_status(stream, nullptr, status);
+}
+
 void mla_decode_mxfp4_release(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   int prev = -1;

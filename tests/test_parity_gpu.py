@@ -252,6 +252,8 @@ def test_malformed_indptr_is_flagged_and_in_bounds():
     d.kv_indptr = torch.tensor([0, 50, 20], dtype=torch.int32)  # decreasing: clamped to rows < 20
     out, st = gpu_decode(d)
     assert st & 1
+    from mla_decode_attention_mxfp4_gb300 import _lib
+    assert _lib.mla_decode_mxfp4_last_device_status() & 1  # the library workspace's status word
     ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, torch.tensor([0, 20, 20], dtype=torch.int32), d.sm_scale)
     check_close(as64(out), ref, "clamped")
 
