@@ -11,8 +11,9 @@
 //
 //  1. mla_partition_kernel: its first CTA sanitises kv_indptr, cuts the concatenated
 //     token stream [indptr[0], indptr[B]) into G equal contiguous ranges (one per
-//     resident CTA), and records, per sequence, which ranges it touches and where
-//     its partial results go; the other CTAs build each sequence's query operand
+//     resident CTA), and writes one work descriptor per range (partial slots are
+//     fixed by range, so the merge derives them from kv_indptr); the other CTAs
+//     build each sequence's query operand
 //     (e4m3 hi/lo parts of the prescaled query, in its shared-memory image) and
 //     the per-head score factors.
 //  2. mla_split_kernel (G persistent CTAs, one per SM): each CTA walks its range in
@@ -35,7 +36,7 @@
 //     mbarriers only, so tile k+1's dequant overlaps tile k's QK^T, softmax and P.V.
 //     A segment that is a whole sequence writes bf16 output directly; otherwise
 //     it writes a normalised fp32 partial and its log2-sum-exp.
-//  3. mla_merge_kernel (one CTA per sequence, one warp per head): merges the
+//  3. mla_merge_kernel (four CTAs per sequence, one warp per head): merges the
 //     partials of split sequences with weights 2^(lse_s - max lse); empty
 //     sequences get zeros.
 //
