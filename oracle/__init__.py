@@ -26,12 +26,16 @@ HEADS, QK, V, PACKED, NSCALE = 16, 576, 512, 288, 18
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with the host C compiler (portable flags only)."""
+    """Compile the oracle with the host C compiler (portable flags only; OpenMP for the
+    multi-threaded driver when the compiler has it, else a single-threaded build)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c99", "-fno-fast-math",
-                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        base = ["gcc", "-O2", "-fPIC", "-shared", "-std=gnu99", "-fno-fast-math", "-ffp-contract=off"]
+        try:
+            subprocess.check_call(base + ["-fopenmp", _SRC, "-o", tmp, "-lm"], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + [_SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -60,6 +64,20 @@ def lib():
         _lib.mxo_decode.argtypes = [u16p, u8p, u8p, i32p, i, d, dp]
         _lib.mxo_decode_split.restype = i
         _lib.mxo_decode_split.argtypes = [u16p, u8p, u8p, i32p, i, d, i, dp]
+        _lib.mxo_decode_mt.restype = i
+        _lib.mxo_decode_mt.argtypes = [u16p, u8p, u8p, i32p, i, d, dp, i]
+        _lib.mxo_decode_rows.restype = i
+        _lib.mxo_decode_rows.argtypes = [u16p, u8p, u8p, i32p, i32p, i, d, dp]
+        _lib.mxo_decode_paged.restype = i
+        _lib.mxo_decode_paged.argtypes = [u16p, u8p, u8p, i32p, i32p, i32p, i32p, i, i, d, dp]
+        _lib.mxo_e4m3.restype = d
+        _lib.mxo_e4m3.argtypes = [i]
+        _lib.mxo_decode_fp8.restype = i
+        _lib.mxo_decode_fp8.argtypes = [u16p, u8p, d, i32p, i, d, dp]
+        _lib.mxo_max_threads.restype = i
+        _lib.mxo_max_threads.argtypes = []
+        _lib.mxo_online_cpus.restype = i
+        _lib.mxo_online_cpus.argtypes = []
     return _lib
 
 
@@ -127,6 +145,31 @@ def decode(q, kv_packed, kv_scale, kv_indptr, sm_scale: float) -> np.ndarray:
     return out
 
 
+def max_threads() -> int:
+    """Threads the multi-threaded driver uses by default (1 in a build without OpenMP)."""
+    return int(lib().mxo_max_threads())
+
+
+def online_cpus() -> int:
+    return int(lib().mxo_online_cpus())
+
+
+def decode_mt(q, kv_packed, kv_scale, kv_indptr, sm_scale: float, nthreads: int | None = None) -> np.ndarray:
+    """decode() with its (sequence, head) pairs on `nthreads` threads (default: all the
+    OpenMP runtime offers); every element is computed exactly as decode() computes it."""
+    qa = _np(q, np.uint16).reshape(-1, HEADS, QK)
+    p = _np(kv_packed, np.uint8).reshape(-1, PACKED)
+    s = _np(kv_scale, np.uint8).reshape(-1, NSCALE)
+    ip = _np(kv_indptr, np.int32)
+    B = ip.shape[0] - 1
+    out = np.zeros((B, HEADS, V), dtype=np.float64)
+    n = max_threads() if nthreads is None else int(nthreads)
+    rc = lib().mxo_decode_mt(_ptr(qa), _ptr(p), _ptr(s), _ptr(ip), B, float(sm_scale), _ptr(out), n)
+    if rc:
+        raise MemoryError(f"oracle decode failed ({rc})")
+    return out
+
+
 def decode_one(q, kv_packed, kv_scale, kv_indptr, sm_scale: float, b: int) -> np.ndarray:
     """Output of sequence `b` only ([16,512] float64); for sampled checks at full size."""
     qa = _np(q, np.uint16).reshape(-1, HEADS, QK)
@@ -153,4 +196,56 @@ def decode_split(q, kv_packed, kv_scale, kv_indptr, sm_scale: float, nsplit: int
                                 int(nsplit), _ptr(out))
     if rc:
         raise RuntimeError(f"oracle split decode failed ({rc})")
+    return out
+
+
+def decode_rows(q, kv_packed, kv_scale, qo_indptr, kv_indptr, sm_scale: float) -> np.ndarray:
+    """Several query rows per sequence: q [total_q,16,576]; rows [qo_indptr[b], qo_indptr[b+1])
+    attend to KV rows [kv_indptr[b], kv_indptr[b+1]).  Returns out [total_q,16,512] float64."""
+    qa = _np(q, np.uint16).reshape(-1, HEADS, QK)
+    p = _np(kv_packed, np.uint8).reshape(-1, PACKED)
+    s = _np(kv_scale, np.uint8).reshape(-1, NSCALE)
+    qo = _np(qo_indptr, np.int32)
+    ip = _np(kv_indptr, np.int32)
+    out = np.zeros((qa.shape[0], HEADS, V), dtype=np.float64)
+    rc = lib().mxo_decode_rows(_ptr(qa), _ptr(p), _ptr(s), _ptr(qo), _ptr(ip), ip.shape[0] - 1, float(sm_scale),
+                               _ptr(out))
+    if rc:
+        raise MemoryError("oracle decode_rows failed")
+    return out
+
+
+def decode_paged(q, kv_packed, kv_scale, kv_indptr, kv_indices, kv_last_page_len, page_size: int,
+                 sm_scale: float, qo_indptr=None) -> np.ndarray:
+    """Paged KV: kv_indptr [B+1] over kv_indices (page ids); kv_packed/kv_scale hold
+    num_pages * page_size rows.  One query row per sequence unless qo_indptr is given."""
+    qa = _np(q, np.uint16).reshape(-1, HEADS, QK)
+    p = _np(kv_packed, np.uint8).reshape(-1, PACKED)
+    s = _np(kv_scale, np.uint8).reshape(-1, NSCALE)
+    ip = _np(kv_indptr, np.int32)
+    ix = _np(kv_indices, np.int32) if np.asarray(kv_indices).size else np.zeros(1, np.int32)
+    last = _np(kv_last_page_len, np.int32) if np.asarray(kv_last_page_len).size else np.zeros(1, np.int32)
+    qo = _np(qo_indptr, np.int32) if qo_indptr is not None else None
+    out = np.zeros((qa.shape[0], HEADS, V), dtype=np.float64)
+    rc = lib().mxo_decode_paged(_ptr(qa), _ptr(p), _ptr(s), _ptr(qo) if qo is not None else None, _ptr(ip),
+                                _ptr(ix), _ptr(last), int(page_size), ip.shape[0] - 1, float(sm_scale), _ptr(out))
+    if rc:
+        raise MemoryError("oracle decode_paged failed")
+    return out
+
+
+def e4m3(byte: int) -> float:
+    return lib().mxo_e4m3(int(byte))
+
+
+def decode_fp8(q, kv_fp8, kv_scale: float, kv_indptr, sm_scale: float) -> np.ndarray:
+    """fp8 (e4m3, no infinities) KV with one per-tensor scale: kv_fp8 [rows,576] bytes."""
+    qa = _np(q, np.uint16).reshape(-1, HEADS, QK)
+    kv = _np(kv_fp8, np.uint8).reshape(-1, QK)
+    ip = _np(kv_indptr, np.int32)
+    B = ip.shape[0] - 1
+    out = np.zeros((B, HEADS, V), dtype=np.float64)
+    rc = lib().mxo_decode_fp8(_ptr(qa), _ptr(kv), float(kv_scale), _ptr(ip), B, float(sm_scale), _ptr(out))
+    if rc:
+        raise MemoryError("oracle decode_fp8 failed")
     return out

@@ -27,6 +27,10 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define MXO_HEADS 16
 #define MXO_QK 576
@@ -92,13 +96,22 @@ void mxo_dequant_token(const uint8_t* packed, const uint8_t* scale, double* k) {
   }
 }
 
+int mxo_attend_heads(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                     int64_t row0, int64_t row1, double sm_scale, int h0, int h1, double* out);
+
 /* Attention of all 16 heads of one query row over KV rows [row0, row1).
  * q: 16*576 bf16 bits; out: 16*512 doubles.  Returns 0, or -1 on allocation
  * failure. */
 int mxo_attend(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
                int64_t row0, int64_t row1, double sm_scale, double* out) {
+  return mxo_attend_heads(q, kv_packed, kv_scale, row0, row1, sm_scale, 0, MXO_HEADS, out);
+}
+
+/* Heads [h0, h1) of the above (out rows of the other heads are left untouched). */
+int mxo_attend_heads(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                     int64_t row0, int64_t row1, double sm_scale, int h0, int h1, double* out) {
   int64_t n = row1 - row0;
-  memset(out, 0, sizeof(double) * MXO_HEADS * MXO_V);
+  memset(out + (size_t)h0 * MXO_V, 0, sizeof(double) * (size_t)(h1 - h0) * MXO_V);
   if (n <= 0) return 0;
   double* k = (double*)malloc(sizeof(double) * (size_t)n * MXO_QK);
   double* s = (double*)malloc(sizeof(double) * (size_t)n);
@@ -110,7 +123,7 @@ int mxo_attend(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_sc
   for (int64_t t = 0; t < n; ++t)
     mxo_dequant_token(kv_packed + (row0 + t) * MXO_PACKED, kv_scale + (row0 + t) * MXO_NSCALE,
                       k + t * MXO_QK);
-  for (int h = 0; h < MXO_HEADS; ++h) {
+  for (int h = h0; h < h1; ++h) {
     double qd[MXO_QK];
     for (int d = 0; d < MXO_QK; ++d) qd[d] = mxo_bf16_to_double(q[h * MXO_QK + d]);
     double m = -INFINITY;
@@ -148,6 +161,158 @@ int mxo_decode(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_sc
     int rc = mxo_attend(q + (size_t)b * MXO_HEADS * MXO_QK, kv_packed, kv_scale, kv_indptr[b],
                         kv_indptr[b + 1], sm_scale, out + (size_t)b * MXO_HEADS * MXO_V);
     if (rc) return rc;
+  }
+  return 0;
+}
+
+/* The same decode with the (sequence, head) pairs spread over `nthreads` OpenMP
+ * threads (each pair runs the single-threaded code above for one head, so every
+ * output element is computed by exactly the same operations in the same order).
+ * Built without OpenMP it runs on one thread.  Returns 0, or -1 on allocation
+ * failure. */
+
+int mxo_decode_mt(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                  const int32_t* kv_indptr, int batch, double sm_scale, double* out, int nthreads) {
+  int rc = 0;
+  if (nthreads < 1) nthreads = 1;
+  /* a whole sequence per task when there are enough sequences (the dequantised rows
+   * are then shared by its 16 heads), else one task per (sequence, head) */
+  const int per_head = batch < 2 * nthreads;
+  const int64_t tasks = per_head ? (int64_t)batch * MXO_HEADS : batch;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : rc)
+#endif
+  for (int64_t i = 0; i < tasks; ++i) {
+    const int b = per_head ? (int)(i / MXO_HEADS) : (int)i;
+    const int h0 = per_head ? (int)(i % MXO_HEADS) : 0, h1 = per_head ? h0 + 1 : MXO_HEADS;
+    rc |= mxo_attend_heads(q + (size_t)b * MXO_HEADS * MXO_QK, kv_packed, kv_scale, kv_indptr[b],
+                           kv_indptr[b + 1], sm_scale, h0, h1, out + (size_t)b * MXO_HEADS * MXO_V);
+  }
+  return rc;
+}
+
+/* Threads an OpenMP region would use by default (1 without OpenMP), and the host's
+ * online processors. */
+int mxo_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+int mxo_online_cpus(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
+
+/* ---- query rows, paged KV, fp8 KV --------------------------------------------
+ * Several query rows per sequence (676098, "_naive_fallback": q rows [qo_indptr[b],
+ * qo_indptr[b+1]) of sequence b each attend, with no mask, to all of b's KV rows).
+ * q [total_q,16,576], out [total_q,16,512]. */
+int mxo_decode_rows(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                    const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, double sm_scale,
+                    double* out) {
+  for (int b = 0; b < batch; ++b) {
+    for (int r = qo_indptr[b]; r < qo_indptr[b + 1]; ++r) {
+      int rc = mxo_attend(q + (size_t)r * MXO_HEADS * MXO_QK, kv_packed, kv_scale, kv_indptr[b],
+                          kv_indptr[b + 1], sm_scale, out + (size_t)r * MXO_HEADS * MXO_V);
+      if (rc) return rc;
+    }
+  }
+  return 0;
+}
+
+/* Paged KV (676098, "_aiter_mla_decode": kv_indptr counts pages of kv_indices, kv_last_page_len
+ * the rows used in each sequence's last page): sequence b's KV rows are, in order, rows
+ * page * page_size + o of its pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]), o < page_size
+ * for every page but the last and o < kv_last_page_len[b] for the last.  The attention is
+ * then the one above over those rows, gathered into a contiguous copy. */
+int mxo_decode_paged(const uint16_t* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                     const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     const int32_t* kv_last_page_len, int page_size, int batch, double sm_scale,
+                     double* out) {
+  for (int b = 0; b < batch; ++b) {
+    const int npages = kv_indptr[b + 1] - kv_indptr[b];
+    const int64_t n = npages > 0 ? (int64_t)(npages - 1) * page_size + kv_last_page_len[b] : 0;
+    uint8_t* gp = (uint8_t*)malloc((size_t)(n > 0 ? n : 1) * MXO_PACKED);
+    uint8_t* gs = (uint8_t*)malloc((size_t)(n > 0 ? n : 1) * MXO_NSCALE);
+    if (!gp || !gs) {
+      free(gp);
+      free(gs);
+      return -1;
+    }
+    for (int64_t t = 0; t < n; ++t) {
+      const int64_t row = (int64_t)kv_indices[kv_indptr[b] + t / page_size] * page_size + t % page_size;
+      memcpy(gp + t * MXO_PACKED, kv_packed + row * MXO_PACKED, MXO_PACKED);
+      memcpy(gs + t * MXO_NSCALE, kv_scale + row * MXO_NSCALE, MXO_NSCALE);
+    }
+    const int r0 = qo_indptr ? qo_indptr[b] : b, r1 = qo_indptr ? qo_indptr[b + 1] : b + 1;
+    int rc = 0;
+    for (int r = r0; r < r1 && rc == 0; ++r)
+      rc = mxo_attend(q + (size_t)r * MXO_HEADS * MXO_QK, gp, gs, 0, n, sm_scale,
+                      out + (size_t)r * MXO_HEADS * MXO_V);
+    free(gp);
+    free(gs);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
+/* fp8 e4m3 ("fn": no infinities) byte -> value, from the format's fields: sign bit 7,
+ * exponent bits 6..3 with bias 7, mantissa bits 2..0; exponent 0 is subnormal
+ * (mantissa / 8 * 2^-6); exponent 15 with mantissa 7 is NaN (so 448 is the largest). */
+double mxo_e4m3(int byte) {
+  const int b = byte & 255, sign = b >> 7, ex = (b >> 3) & 15, man = b & 7;
+  double mag;
+  if (ex == 15 && man == 7) return NAN;
+  if (ex == 0) mag = ldexp((double)man, -9);
+  else mag = ldexp(1.0 + man / 8.0, ex - 7);
+  return sign ? -mag : mag;
+}
+
+/* fp8 KV with one per-tensor scale (676098 "_aiter_mla_decode", 717900 "_decode"):
+ * K[t][d] = e4m3(kv[t][d]) * kv_scale, V = K[:, :512]; the query is used as given (bf16).
+ * kv [rows,576] bytes. */
+int mxo_decode_fp8(const uint16_t* q, const uint8_t* kv, double kv_scale, const int32_t* kv_indptr,
+                   int batch, double sm_scale, double* out) {
+  for (int b = 0; b < batch; ++b) {
+    const int64_t r0 = kv_indptr[b], n = kv_indptr[b + 1] - r0;
+    double* o = out + (size_t)b * MXO_HEADS * MXO_V;
+    memset(o, 0, sizeof(double) * MXO_HEADS * MXO_V);
+    if (n <= 0) continue;
+    double* k = (double*)malloc(sizeof(double) * (size_t)n * MXO_QK);
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    if (!k || !s) {
+      free(k);
+      free(s);
+      return -1;
+    }
+    for (int64_t t = 0; t < n; ++t)
+      for (int d = 0; d < MXO_QK; ++d) k[t * MXO_QK + d] = mxo_e4m3(kv[(r0 + t) * MXO_QK + d]) * kv_scale;
+    for (int h = 0; h < MXO_HEADS; ++h) {
+      double qd[MXO_QK];
+      for (int d = 0; d < MXO_QK; ++d) qd[d] = mxo_bf16_to_double(q[((size_t)b * MXO_HEADS + h) * MXO_QK + d]);
+      double m = -INFINITY;
+      int any_nan = 0;
+      for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int d = 0; d < MXO_QK; ++d) dot += qd[d] * k[t * MXO_QK + d];
+        s[t] = sm_scale * dot;
+        if (isnan(s[t])) any_nan = 1;
+        else if (s[t] > m) m = s[t];
+      }
+      double* oh = o + h * MXO_V;
+      if (any_nan) {
+        for (int d = 0; d < MXO_V; ++d) oh[d] = NAN;
+        continue;
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < n; ++t) {
+        const double w = exp(s[t] - m);
+        l += w;
+        for (int d = 0; d < MXO_V; ++d) oh[d] += w * k[t * MXO_QK + d];
+      }
+      for (int d = 0; d < MXO_V; ++d) oh[d] /= l;
+    }
+    free(k);
+    free(s);
   }
   return 0;
 }

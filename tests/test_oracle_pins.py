@@ -229,3 +229,15 @@ def test_sharp_softmax_selects_the_aligned_token():
     for h in range(16):
         best = int(np.argmax(k @ qf[h]))
         assert np.array_equal(out[0, h], k[best, :512])
+
+
+@pytest.mark.parametrize("nthreads", [1, 3, 8])
+def test_multithreaded_driver_is_bitwise_the_single_threaded_oracle(nthreads):
+    """The OpenMP driver (used for full-size parity and the multi-core CPU baseline) runs
+    the same per-head arithmetic: identical bits for every element, empty sequences and
+    the (sequence, head) task split included."""
+    for lens in ([5, 0, 3], [1] * 40, [70, 2, 0, 0, 33]):
+        d = MI.make_custom(lens, seed=len(lens))
+        a = oracle.decode(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, SM)
+        b = oracle.decode_mt(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, SM, nthreads)
+        assert np.array_equal(a.view(np.int64), b.view(np.int64))
