@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -82,12 +83,12 @@ class ClockSampler:
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="mla_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "50", "-i", self.gpu_id], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -104,7 +105,10 @@ class ClockSampler:
         self.fh.close()
         rows = []
         with open(self.path) as f:
-            for line in f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        if True:
+            for line in lines:
                 parts = [x.strip() for x in line.split(",")]
                 if len(parts) < 10:
                     continue
@@ -156,9 +160,17 @@ def _workload_desc(name, d):
 
 
 def cpu_baseline(d, budget_s=10.0):
-    """The fp64 oracle, as it stands, on a bounded sample of whole sequences."""
+    """The fp64 oracle, as it stands, on the host cores: the whole call on every core the
+    OpenMP runtime offers (its (sequence, head) driver), and beside it the single-threaded
+    oracle on a bounded sample of whole sequences."""
     import oracle
     oracle.build()
+    nthreads = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while reps < 1 or (time.perf_counter() - t0 < budget_s / 4 and reps < 5):
+        oracle.decode_mt(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale, nthreads)
+        reps += 1
+    mt_s = (time.perf_counter() - t0) / reps
     t0 = time.perf_counter()
     done_tokens, done_seqs, done_bytes = 0, 0, 0
     B = d.batch
@@ -170,52 +182,53 @@ def cpu_baseline(d, budget_s=10.0):
         done_bytes += 18432 + n * 306 + 16384
         done_seqs += 1
     el = time.perf_counter() - t0
-    full_s = el * d.algorithmic_bytes() / done_bytes
-    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "us_per_call": full_s * 1e6,
-            "sample": f"{done_seqs} of {B} sequences ({done_tokens} tokens) decoded by the single-threaded "
-                      f"fp64 C oracle in {el:.2f} s; us_per_call extrapolated by bytes"}
+    return {"value": d.algorithmic_bytes() / mt_s / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "us_per_call": mt_s * 1e6, "online_cpus": oracle.online_cpus(),
+            "sample": f"the whole call ({B} sequences, {d.total_kv} tokens) decoded {reps}x by the fp64 C oracle's "
+                      f"OpenMP driver over (sequence, head) on {nthreads} threads",
+            "single_thread": {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": 1,
+                              "us_per_call": el * d.algorithmic_bytes() / done_bytes * 1e6,
+                              "sample": f"{done_seqs} of {B} sequences ({done_tokens} tokens) in {el:.2f} s; "
+                                        "us_per_call extrapolated by bytes"}}
 
 
 def run_reference(args):
     ws, rank, _ = _dist_env()
     if rank != 0:
         return
-    import torch
-
     import mla_inputs as MI
     import oracle
     oracle.build()
     d = MI.make_inputs(args.workload)
-    # calibrate a per-step sample so the whole run stays within ~2 minutes
-    n0 = int(d.kv_indptr[1] - d.kv_indptr[0])
-    t = time.perf_counter()
-    oracle.decode_one(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale, 0)
-    per_token = (time.perf_counter() - t) / max(n0, 1)
+    nthreads = oracle.max_threads()
+    # calibrate a per-step sample of leading sequences so the whole run stays within ~2 minutes
     steps_total = args.steps + args.warmup
-    tok_budget = max(16, min(n0, int(120.0 / steps_total / per_token)))
-    ip = torch.tensor([0, tok_budget], dtype=torch.int32)
+    t = time.perf_counter()
+    oracle.decode_mt(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale, nthreads)
+    full_s = time.perf_counter() - t
+    nseq = d.batch
+    while nseq > 1 and full_s * nseq / d.batch * steps_total > 120.0:
+        nseq = max(1, nseq // 2)
+    ip = d.kv_indptr[:nseq + 1]
+    rows = int(ip[-1])
+    q, kv, sc = d.q[:nseq], d.kv_packed[:rows], d.kv_scale[:rows]
+    nbytes = nseq * (18432 + 16384) + rows * 306
     times = []
     for i in range(steps_total):
-        bb = i % d.batch
-        r0 = int(d.kv_indptr[bb])
-        n = min(tok_budget, int(d.kv_indptr[bb + 1]) - r0)
-        ipb = torch.tensor([0, n], dtype=torch.int32) if n != tok_budget else ip
-        kv, sc = d.kv_packed[r0:r0 + n], d.kv_scale[r0:r0 + n]
         t = time.perf_counter()
-        oracle.decode(d.q[bb:bb + 1], kv, sc, ipb, d.sm_scale)
+        oracle.decode_mt(q, kv, sc, ip, d.sm_scale, nthreads)
         if i >= args.warmup:
-            times.append((time.perf_counter() - t, 18432 + n * 306 + 16384))
-    step_s = sum(x for x, _ in times) / len(times)
-    val = sum(b for _, b in times) / sum(x for x, _ in times) / 1e9
+            times.append(time.perf_counter() - t)
+    step_s = sum(times) / len(times)
+    val = nbytes / step_s / 1e9
     line = {"impl": "reference", "metric": "MLA decode achieved HBM GB/s (and us/call)", "value": val,
             "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": _workload_desc(args.workload, d),
-            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: sequence (step mod batch), first {tok_budget} tokens, "
-                                       "single-threaded fp64 C oracle"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"each step: the first {nseq} of {d.batch} sequences ({rows} tokens) "
+                                       f"decoded by the fp64 C oracle's OpenMP driver on {nthreads} threads"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -237,6 +250,78 @@ def whole_job_gbps(world, nbytes_per_rank, ms):
     return world * nbytes_per_rank / (ms * 1e-3) / 1e9
 
 
+class DeviceWorkload:
+    """One workload's inputs resident in HBM (rotated over enough copies that the working set
+    exceeds L2) and one decode call through the C ABI with a caller-owned workspace."""
+
+    def __init__(self, d, dev, stream):
+        import torch
+
+        from mla_decode_attention_mxfp4_gb300 import _lib, alloc_workspace
+        self.d, self.dev, self.stream, self._lib = d, dev, stream, _lib
+        self.nbytes = d.algorithmic_bytes()
+        # the split kernel's own algorithmic bytes: every KV row and every query once (the
+        # output of split sequences is written by the merge kernel)
+        self.split_bytes = d.total_kv * 306 + d.batch * 18432
+        self.in_bytes = d.q.numel() * 2 + d.kv_packed.numel() + d.kv_scale.numel()
+        self.copies = max(2, min(8, math.ceil(4 * L2_BYTES / self.in_bytes)))
+        self.bufs = [(d.q.to(dev), d.kv_packed.to(dev), d.kv_scale.to(dev), d.kv_indptr.to(dev),
+                      torch.empty(d.batch, 16, 512, dtype=torch.bfloat16, device=dev)) for _ in range(self.copies)]
+        self.ws = alloc_workspace(d.batch, dev)
+        torch.cuda.synchronize(dev)
+
+    def l2_note(self):
+        return (f"timed calls rotate over {self.copies} input copies "
+                f"({self.copies * self.in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES // 2**20} MiB)")
+
+    def call(self, i, ev_b=None, ev_e=None):
+        q, kv, sc, ip, out = self.bufs[i % self.copies]
+        rc = self._lib.mla_decode_mxfp4_ws_timed(q.data_ptr(), kv.data_ptr(), sc.data_ptr(), ip.data_ptr(),
+                                                 out.data_ptr(), self.d.batch, self.d.sm_scale,
+                                                 self.stream.cuda_stream, self.ws.data_ptr(), self.ws.numel(),
+                                                 ev_b, ev_e)
+        if rc != 0:
+            raise RuntimeError(self._lib.status_string(rc))
+
+    def time_calls(self, steps):
+        """Mean device time of `steps` back-to-back calls (CUDA events on the launching stream)."""
+        import torch
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for i in range(steps):
+            self.call(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) / steps
+
+    def time_split_kernel(self, steps):
+        """Mean duration of the split kernel alone: events recorded around it by the library,
+        on the stream it is launched on, over the same rotation of inputs."""
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(steps, 400))]
+        for a, b in evs:  # torch creates the CUDA events lazily, at the first record
+            a.record(self.stream)
+            b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        for i, (a, b) in enumerate(evs):
+            self.call(i, a.cuda_event, b.cuda_event)
+        torch.cuda.synchronize(self.dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    def roofline(self, split_ms, peak, peak_src, workload):
+        achieved = self.split_bytes / (split_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "mla_split_kernel", "achieved": achieved, "peak": peak,
+                "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                "split_kernel_us": split_ms * 1e3, "split_kernel_bytes": self.split_bytes,
+                "traffic": _traffic_per_launch(workload)}
+
+
+NUMERICS = ("K/V as e5m2 (exact e2m1*2^k per token, 13 binades of headroom), query and P as two e4m3 "
+            "terms each, tcgen05 f8f6f4 MMAs with fp32 accumulation, fp32 softmax and merge, bf16 out")
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -250,27 +335,11 @@ def run_native(args):
     import __graft_entry__
     __graft_entry__.build()
     import mla_inputs as MI
-    from mla_decode_attention_mxfp4_gb300 import HostDecoder, _lib, alloc_workspace
+    from mla_decode_attention_mxfp4_gb300 import HostDecoder
 
-    d = MI.make_inputs(args.workload)
-    nbytes = d.algorithmic_bytes()
-    in_bytes = d.q.numel() * 2 + d.kv_packed.numel() + d.kv_scale.numel()
-    copies = max(2, min(8, math.ceil(4 * L2_BYTES / in_bytes)))
     stream = torch.cuda.Stream(dev)
-    bufs = []
-    for _ in range(copies):
-        bufs.append((d.q.to(dev), d.kv_packed.to(dev), d.kv_scale.to(dev), d.kv_indptr.to(dev),
-                     torch.empty(d.batch, 16, 512, dtype=torch.bfloat16, device=dev)))
-    wsb = alloc_workspace(d.batch, dev)
-    torch.cuda.synchronize(dev)
-
-    def call(i, ev_b=None, ev_e=None):
-        q, kv, sc, ip, out = bufs[i % copies]
-        rc = _lib.mla_decode_mxfp4_ws_timed(q.data_ptr(), kv.data_ptr(), sc.data_ptr(), ip.data_ptr(), out.data_ptr(),
-                                            d.batch, d.sm_scale, stream.cuda_stream, wsb.data_ptr(), wsb.numel(),
-                                            ev_b, ev_e)
-        if rc != 0:
-            raise RuntimeError(_lib.status_string(rc))
+    d = MI.make_inputs(args.workload)
+    W = DeviceWorkload(d, dev, stream)
 
     def barrier():
         if ws > 1:
@@ -280,40 +349,25 @@ def run_native(args):
     sampler.start()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            call(i)
+            W.call(i)
         # untimed soak (~1 s) so the clock sampler sees the load
         torch.cuda.synchronize(dev)
         t_end = time.time() + 1.0
         i = 0
         while time.time() < t_end:
             for _ in range(200):
-                call(i)
+                W.call(i)
                 i += 1
             torch.cuda.synchronize(dev)
         # ---- timed region: exactly K steps ----
         barrier()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.time()
-        e0.record(stream)
-        for i in range(args.steps):
-            call(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms = W.time_calls(args.steps)
         wall1 = time.time()
         barrier()
-        ms = e0.elapsed_time(e1) / args.steps
         # ---- split-kernel-only timing (same rotation, events around that kernel) ----
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(min(args.steps, 400))]
-        for a, b in evs:  # torch creates the CUDA events lazily, at the first record
-            a.record(stream)
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        for i, (a, b) in enumerate(evs):
-            call(i, a.cuda_event, b.cuda_event)
-        torch.cuda.synchronize(dev)
-        split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        split_ms = W.time_split_kernel(args.steps)
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows, wall0, wall1)
 
@@ -322,9 +376,9 @@ def run_native(args):
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(copies):
-                call(i)
-        reps = max(1, args.steps // copies)
+            for i in range(W.copies):
+                W.call(i)
+        reps = max(1, args.steps // W.copies)
         with torch.cuda.stream(stream):  # replay() launches on the current stream
             g.replay()
             torch.cuda.synchronize(dev)
@@ -334,7 +388,7 @@ def run_native(args):
                 g.replay()
             gb.record(stream)
         torch.cuda.synchronize(dev)
-        graph_ms = ga.elapsed_time(gb) / (reps * copies)
+        graph_ms = ga.elapsed_time(gb) / (reps * W.copies)
     except Exception as exc:  # reported, not fatal
         graph_ms = f"unavailable: {exc}"
 
@@ -357,36 +411,51 @@ def run_native(args):
     e2e_ms = ea.elapsed_time(eb) / e2e_steps
     barrier()
 
+    # ---- the other gated workload(s): device-timed the same way, rank 0 reports them ----
+    peak, peak_src = _peaks()
+    extra = {}
+    for name in args.extra:
+        if name == args.workload:
+            continue
+        dx = MI.make_inputs(name)
+        X = DeviceWorkload(dx, dev, stream)
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, 10)):
+                X.call(i)
+            xs = max(args.steps, 20)
+            xms = X.time_calls(xs)
+            xsplit = X.time_split_kernel(xs)
+        extra[name] = {"config": dict(_workload_desc(name, dx), l2=X.l2_note()),
+                       "value": whole_job_gbps(ws, X.nbytes, xms), "unit": "GB/s", "us_per_call": xms * 1e3,
+                       "frac_of_hbm_peak": X.nbytes / (xms * 1e-3) / 1e9 / peak, "steps": xs,
+                       "roofline": X.roofline(xsplit, peak, peak_src, name)}
+        del X
+        torch.cuda.empty_cache()
+
     ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], dev)
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
         return
-    peak, peak_src = _peaks()
-    achieved = nbytes / (split_ms * 1e-3) / 1e9
     line = {
         "metric": "MLA decode achieved HBM GB/s (and us/call)",
-        "value": whole_job_gbps(ws, nbytes, ms),
+        "value": whole_job_gbps(ws, W.nbytes, ms),
         "unit": "GB/s",
         "us_per_call": ms * 1e3,
-        "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+        "frac_of_hbm_peak": W.nbytes / (ms * 1e-3) / 1e9 / peak,
         "us_per_call_graph": graph_ms * 1e3 if isinstance(graph_ms, float) else graph_ms,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8", "data": "synthetic",
-        "config": dict(_workload_desc(args.workload, d),
-                       l2=f"timed calls rotate over {copies} input copies "
-                          f"({copies * in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES // 2**20} MiB)",
+        "dtype": "fp8 operands, fp32 accumulate", "numerics": NUMERICS, "data": "synthetic",
+        "config": dict(_workload_desc(args.workload, d), l2=W.l2_note(),
                        parallelism=f"replica per GPU x{ws}" if ws > 1 else "1 GPU"),
-        "roofline": {"bound": "hbm", "kernel": "mla_split_kernel", "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                     "split_kernel_us": split_ms * 1e3,
-                     "traffic": _traffic_per_launch(args.workload)},
-        "e2e": {"value": whole_job_gbps(ws, nbytes, e2e_ms), "unit": "GB/s", "us_per_call": e2e_ms * 1e3,
-                "h2d_bytes_per_step": in_bytes + d.kv_indptr.numel() * 4,
+        "roofline": W.roofline(split_ms, peak, peak_src, args.workload),
+        "e2e": {"value": whole_job_gbps(ws, W.nbytes, e2e_ms), "unit": "GB/s", "us_per_call": e2e_ms * 1e3,
+                "h2d_bytes_per_step": W.in_bytes + d.kv_indptr.numel() * 4,
                 "d2h_bytes_per_step": d.batch * 16 * 512 * 2},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "extra_workloads": extra,
     }
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d)
@@ -403,6 +472,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="uniform")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", nargs="*", default=["ragged"],
+                    help="further workloads measured on the device and reported under extra_workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

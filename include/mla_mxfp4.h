@@ -109,6 +109,20 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
                               mla_stream_t stream, void* workspace, size_t ws_bytes,
                               void* ev_split_begin, void* ev_split_end);
 
+/* Test-only variant of mla_decode_mxfp4_ws that exercises the failure path of the
+ * attention kernel's bounded waits without faulting anything: the kernel's copy
+ * role issues no copy at all, so the first wait for a landed tile runs out after
+ * `timeout_ns` nanoseconds of global time (1 .. 1e9; other values return
+ * MLA_ERR_BAD_SCALE).  Every role then stops issuing asynchronous work, drains what
+ * it issued and runs to its end; the call completes, `out` holds unspecified
+ * values, and the workspace's device status word has MLA_DEVICE_TIMEOUT set.  The
+ * context stays usable.  Same arguments, ownership and errors otherwise as
+ * mla_decode_mxfp4_ws. */
+int mla_decode_mxfp4_ws_stalled(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                                const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                                mla_stream_t stream, void* workspace, size_t ws_bytes,
+                                unsigned long long timeout_ns);
+
 /* No-allocation variant of mla_decode_mxfp4, for callers that may not allocate
  * device memory at all: code running inside an allocator or memory-pool
  * callback, processes whose device memory is fully reserved up front by a
@@ -124,19 +138,31 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
  * rejected with MLA_ERR_WORKSPACE before anything is launched.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call on a device shares the one array and it keeps
+ * The array is part of the library's device code, so it is reserved when that
+ * code is loaded onto a device: under CUDA's lazy module loading that is the first
+ * call of any entry point on that device.  The first call of this function on each
+ * device also looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current.  So make one call on each device at start-up, before device
+ * memory is fully reserved and before any stream capture; until then a call can
+ * fail with MLA_ERR_CUDA.  Every call on a device shares the one array and it keeps
  * the previous call's contents; nothing in it needs to start at zero (each call
  * rewrites the metadata it reads), but calls that may overlap on the GPU (other
- * streams, other host threads) race on it and must be ordered by the caller. */
+ * streams, other host threads) race on it and must be ordered by the caller.  The
+ * array's device status word is read with mla_decode_mxfp4_device_status(stream,
+ * MLA_STATIC_SCRATCH, &status). */
 int mla_decode_mxfp4_noalloc(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
                              const int32_t* kv_indptr, void* out, int batch, float sm_scale,
                              mla_stream_t stream);
 
+/* Pass as `workspace` to mla_decode_mxfp4_device_status to read the status word of
+ * the static scratch array that mla_decode_mxfp4_noalloc uses. */
+#define MLA_STATIC_SCRATCH ((const void*)1)
+
 /* Debug: synchronise `stream`, then read the device status word (mla_device_status
  * bits) left by the last call that used `workspace` (NULL = the library workspace
- * of the current device).  Returns MLA_OK or MLA_ERR_CUDA. */
+ * of the current device, MLA_STATIC_SCRATCH = the no-allocation scratch of the
+ * current device).  A workspace no call has used yet reads as 0.  Returns MLA_OK
+ * or MLA_ERR_CUDA. */
 int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, int* status);
 
 /* Same for the library workspace of the current device: the status of the last

@@ -24,6 +24,8 @@ MLA_ERR_WORKSPACE = 5
 MLA_ERR_CUDA = 6
 MLA_DEVICE_BAD_INDPTR = 1
 MLA_DEVICE_TIMEOUT = 2
+# mla_decode_mxfp4_device_status(stream, MLA_STATIC_SCRATCH, ...) reads the no-allocation scratch
+MLA_STATIC_SCRATCH = 1
 
 
 class MlaError(RuntimeError):
@@ -59,6 +61,8 @@ def lib():
     L.mla_decode_mxfp4_ws.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz]
     L.mla_decode_mxfp4_ws_timed.restype = i
     L.mla_decode_mxfp4_ws_timed.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz, vp, vp]
+    L.mla_decode_mxfp4_ws_stalled.restype = i
+    L.mla_decode_mxfp4_ws_stalled.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz, ctypes.c_ulonglong]
     L.mla_decode_mxfp4_workspace_bytes.restype = sz
     L.mla_decode_mxfp4_workspace_bytes.argtypes = [i, i]
     L.mla_decode_mxfp4_device_status.restype = i
@@ -93,6 +97,13 @@ def mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_
                               ws_bytes, ev_split_begin, ev_split_end) -> int:
     return lib().mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, int(batch), float(sm_scale),
                                            stream, workspace, int(ws_bytes), ev_split_begin, ev_split_end)
+
+
+def mla_decode_mxfp4_ws_stalled(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace,
+                                ws_bytes, timeout_ns) -> int:
+    """Test-only: the attention kernel's copy role issues nothing, so its waits run out."""
+    return lib().mla_decode_mxfp4_ws_stalled(q, kv_packed, kv_scale, kv_indptr, out, int(batch), float(sm_scale),
+                                             stream, workspace, int(ws_bytes), int(timeout_ns))
 
 
 def mla_decode_mxfp4_noalloc(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream) -> int:

@@ -106,9 +106,21 @@ int check_args(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
   return MLA_OK;
 }
 
+// Wait limit of the split kernel's mbarrier waits (global time); a wait that runs out
+// raises MLA_DEVICE_TIMEOUT and the launch returns instead of blocking.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+struct LaunchOpts {
+  cudaEvent_t ev_begin = nullptr;  // recorded right before the split kernel
+  cudaEvent_t ev_end = nullptr;    // recorded right after it
+  unsigned long long timeout_ns = kWaitLimitNs;
+  int stall_producer = 0;          // test hook (mla_decode_mxfp4_ws_stalled)
+};
+
 int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, const int32_t* kv_indptr, void* out,
            int batch, float sm_scale, cudaStream_t stream, void* ws, const DeviceInfo& di,
-           cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
+           const LaunchOpts& opt = LaunchOpts()) {
+  const cudaEvent_t ev_begin = opt.ev_begin, ev_end = opt.ev_end;
   const WsOffsets o = ws_offsets(batch, di.grid);
   const mla::Workspace w = ws_bind(ws, o);
   const int kv_null = (kv_packed == nullptr || kv_scale == nullptr) ? 1 : 0;
@@ -137,7 +149,8 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
   sp.out = static_cast<__nv_bfloat16*>(out);
   sp.ws = w;
   sp.B = batch;
-  sp.timeout_ns = 1000000000ull;
+  sp.timeout_ns = opt.timeout_ns;
+  sp.stall_producer = opt.stall_producer;
   // split and merge are launched with programmatic stream serialization: each may be
   // scheduled while its predecessor runs and waits for it with griddepcontrol.wait.  The
   // timed variant records events between the launches, which orders them as usual.
@@ -164,7 +177,9 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
     if (cudaLaunchKernelEx(&cfg, mla::mla_merge_kernel, static_cast<__nv_bfloat16*>(out), w, batch) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  // every launch and event record above was checked; an error left pending on this thread
+  // by unrelated work is not this call's and is left for its owner to read
+  return MLA_OK;
 }
 
 // ---- static scratch for callers that cannot allocate device memory ----------
@@ -190,19 +205,10 @@ void* g_static_ptr[kMaxDevices] = {};
 
 }  // namespace
 
-extern "C" {
-
-size_t mla_decode_mxfp4_workspace_bytes(int batch, int device) {
-  if (batch < 0) return 0;
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceInfo di;
-  if (device_info(device, &di) != MLA_OK) return 0;
-  return ws_offsets(batch, di.grid).total;
-}
-
-int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
-                              const int32_t* kv_indptr, void* out, int batch, float sm_scale, mla_stream_t stream,
-                              void* workspace, size_t ws_bytes, void* ev_split_begin, void* ev_split_end) {
+namespace {
+int launch_ws(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, const int32_t* kv_indptr, void* out,
+              int batch, float sm_scale, mla_stream_t stream, void* workspace, size_t ws_bytes,
+              const LaunchOpts& opt) {
   int rc = check_args(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale);
   if (rc != MLA_OK || batch == 0) return rc;
   if (!workspace) return MLA_ERR_NULL_PTR;
@@ -217,14 +223,46 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
   if (rc != MLA_OK) return rc;
   if (ws_bytes < ws_offsets(batch, di.grid).total) return MLA_ERR_WORKSPACE;
   return launch(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, reinterpret_cast<cudaStream_t>(stream),
-                workspace, di, static_cast<cudaEvent_t>(ev_split_begin), static_cast<cudaEvent_t>(ev_split_end));
+                workspace, di, opt);
+}
+}  // namespace
+
+extern "C" {
+
+size_t mla_decode_mxfp4_workspace_bytes(int batch, int device) {
+  if (batch < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo di;
+  if (device_info(device, &di) != MLA_OK) return 0;
+  return ws_offsets(batch, di.grid).total;
+}
+
+
+int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                              const int32_t* kv_indptr, void* out, int batch, float sm_scale, mla_stream_t stream,
+                              void* workspace, size_t ws_bytes, void* ev_split_begin, void* ev_split_end) {
+  LaunchOpts opt;
+  opt.ev_begin = static_cast<cudaEvent_t>(ev_split_begin);
+  opt.ev_end = static_cast<cudaEvent_t>(ev_split_end);
+  return launch_ws(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace, ws_bytes, opt);
+}
+
+int mla_decode_mxfp4_ws_stalled(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                                const int32_t* kv_indptr, void* out, int batch, float sm_scale,
+                                mla_stream_t stream, void* workspace, size_t ws_bytes,
+                                unsigned long long timeout_ns) {
+  if (timeout_ns == 0 || timeout_ns > kWaitLimitNs) return MLA_ERR_BAD_SCALE;
+  LaunchOpts opt;
+  opt.timeout_ns = timeout_ns;
+  opt.stall_producer = 1;
+  return launch_ws(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace, ws_bytes, opt);
 }
 
 int mla_decode_mxfp4_ws(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
                         const int32_t* kv_indptr, void* out, int batch, float sm_scale, mla_stream_t stream,
                         void* workspace, size_t ws_bytes) {
-  return mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace,
-                                   ws_bytes, nullptr, nullptr);
+  return launch_ws(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace, ws_bytes,
+                   LaunchOpts());
 }
 
 int mla_decode_mxfp4(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, const int32_t* kv_indptr,
@@ -295,15 +333,16 @@ int mla_decode_mxfp4_device_status(mla_stream_t stream, const void* workspace, i
   if (!status) return MLA_ERR_NULL_PTR;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
   const void* ws = workspace;
-  if (!ws) {
+  if (!ws || ws == MLA_STATIC_SCRATCH) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (dev < 0 || dev >= kMaxDevices || !g_ws[dev]) {
+    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+    ws = ws ? g_static_ptr[dev] : g_ws[dev];
+    if (!ws) {  // no call has used it on this device yet
       *status = 0;
       return MLA_OK;
     }
-    ws = g_ws[dev];
   }
   int meta[16];
   if (cudaMemcpy(meta, ws, sizeof(meta), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;

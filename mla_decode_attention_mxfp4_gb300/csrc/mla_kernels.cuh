@@ -24,10 +24,10 @@
 //                   3-stage smem ring, the sequence's query operand into one of two
 //                   buffers at a segment start);
 //       warps 2..5  softmax group, one warp per tensor-memory lane quarter (32
-//                   tokens), all 16 heads: online softmax of S^T, P as e4m3 hi + lo
+//                   tokens), all 16 heads: online softmax of S^T, P as e5m2 hi + lo
 //                   parts, rescaling of the O^T accumulator, segment epilogue;
-//       warps 6..17 dequant group, three warps per lane quarter: per-token scale
-//                   rebasing, the K tile as e5m2 into tensor memory (A operand of
+//       warps 6..17 dequant group, three warps per lane quarter: the tile's
+//                   reference exponent, the K tile as e5m2 into tensor memory (A operand of
 //                   QK^T, double-buffered), V^T as e5m2 into shared memory, the
 //                   score factors at a segment start.
 //     QK^T (S^T[128 tokens][32] = K . Qhat^T, hi and lo query parts stacked as N)
@@ -40,15 +40,20 @@
 //     partials of split sequences with weights 2^(lse_s - max lse); empty
 //     sequences get zeros.
 //
-// Numerics: e2m1 * 2^(s_tb - S_t), S_t the largest scale exponent of token t, has at
-// most two significant bits, so it is exact in e5m2 (the high byte of its fp16 form)
-// for s_tb >= S_t - 15; the token factor 2^(S_t - 127) multiplies the fp32 score and
-// is rebased in P.  The query is q * 2^-E_h (E_h per head) as two e4m3 terms, which
-// hold a bf16 value exactly unless it lies more than 2^11 below its head's maximum.
-// P is rebased against a running maximum that is only raised when the tile maximum
-// exceeds it by more than 2^4 (scores) or 2^4 (token exponents), so
-// P * 2^(S_t - R) <= 256 fits e4m3; it is carried as hi + lo e4m3 parts (about 8
-// significant bits).  Scores, softmax statistics, accumulation and the merge are fp32.
+// Numerics: the K/V operand of tile k is e2m1 * 2^(s_tb - R_k + kHead) in e5m2, with R_k the
+// tile's reference exponent (its largest scale byte, or a little above it, see
+// next_reference) and kHead = 13 the headroom that puts the largest possible element
+// (6 * 2^13 = 49152) just under the e5m2 maximum.  Such a value has at most two
+// significant bits, so it is exact in e5m2 (the high byte of its fp16 form) for
+// s_tb >= R_k - 27; blocks further below are zero.  The tile factor 2^(R_k - 127 - kHead)
+// multiplies the fp32 scores, and the O^T accumulator, which holds P.V against the
+// reference of the latest tile, is rescaled by 2^(R_old - R_new) when the reference changes.
+// The query is q * 2^-E_h (E_h per head) as two e4m3 terms, which hold a bf16 value
+// exactly unless it lies more than 2^11 below its head's maximum.  P = 2^(s - m) uses a
+// running maximum m that is only raised when a tile's maximum exceeds it by more than
+// 2^4, so P <= 16; it enters P.V as two e5m2 terms of 2^11 P (about 6 significant bits for
+// every weight down to ~2^-20 of the largest, so long flat tails of small weights are kept).
+// Scores, softmax statistics, accumulation and the merge are fp32.
 #pragma once
 #include <climits>
 #include <cstdint>
@@ -118,7 +123,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;      // 2 x 144 columns: e5m2 K tile, column c = dims 4c..4c+3
 constexpr uint32_t kColsA = 144;
 constexpr uint32_t kColS = 288;    // 2 x 32 columns: S^T from the hi (0..15) and lo (16..31) query parts
-constexpr uint32_t kColSt = 352;   // 4 columns: S_t of the tile's tokens (tile k in column k % 4)
+constexpr uint32_t kColSt = 352;   // 4 columns: reference exponent R of the tile (tile k in column k % 4, every lane)
 constexpr uint32_t kColO = 384;    // 128 columns: O^T, 4 blocks of 128 dims x (16 hi + 16 lo P parts)
 
 // Qhat, e4m3 hi (n = head) and lo (n = 16 + head) parts, K-major without swizzle:
@@ -127,23 +132,38 @@ constexpr uint32_t kQLbo = 512, kQSbo = 128;
 // V^T, e5m2, MN-major without swizzle, 4 blocks of 128 dims:
 // offset(d, t) = (d/128)*kVtBlock + (t/8)*kVtLbo + ((d%128)/16)*kVtSbo + (t%8)*16 + d%16.
 constexpr uint32_t kVtBlock = 16384, kVtLbo = 1024, kVtSbo = 128;
-// P^T, e4m3, MN-major, two buffers, n = head (hi part) or 16 + head (lo part):
+// P^T, e5m2, MN-major, two buffers, n = head (hi part) or 16 + head (lo part):
 // offset(n, t) = (t/8)*kPtLbo + (n/16)*kPtSbo + (t%8)*16 + n%16.
 constexpr uint32_t kPtLbo = 256, kPtSbo = 128, kPtBytes = kTile * 32;
 constexpr int kMaxThresh = 4;  // raise the running maxima only by more than this (log2 units)
+// Headroom of the K/V operand: a block at the tile's reference exponent is stored as
+// e2m1 * 2^kHead, so its largest possible element 6 * 2^13 = 49152 stays below the e5m2
+// maximum 57344 and blocks down to 27 binades below the reference stay exact (smallest e5m2
+// subnormal: 2^-16).
+constexpr int kHead = 13;
+constexpr float kHeadInv = 1.f / 8192.f;  // 2^-kHead
+static_assert(kHeadInv * (1 << kHead) == 1.f, "headroom factor");
+// P enters P.V as two e5m2 terms of P' = 2^kPExp P (hi = e5m2(P') in O^T columns 0..15 of a
+// block, lo = e5m2(P' - hi) in columns 16..31): about 6 significant bits for every weight from
+// the largest down to ~2^-20 of it (e5m2's exponent range keeps long flat tails of small
+// weights).  The softmax keeps its running maxima as m - kPExp, so P' comes out of ex2 directly;
+// the row sums then hold 2^kPExp l, and the factor cancels in O / l and in m + log2 l.
+constexpr int kPExp = 11;      // P' <= 2^(kPExp + kMaxThresh) = 2^15 < the e5m2 maximum
+constexpr float kOutInv = kHeadInv;
 
 constexpr int kOffStages = 0;
 constexpr int kOffQhat = kOffStages + kStages * kStageBytes;              // 117888: [2] (segment parity)
 constexpr int kOffVt = kOffQhat + 2 * kQhatBytes;                         // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
 constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][16 heads][4 quarters]
-constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: [2][4] token-exponent maxima
+constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: (unused, 32 bytes)
 constexpr int kOffCh = kOffRw + 32;                                       // 229024: [4][16] score factors
 constexpr int kOffLw = kOffCh + 4 * kHeads * 4;                           // 229280: [16 heads][4 quarters]
 constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229536: [16] output factors
 constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229600: [4 warps][16 m, 16 alpha]
-constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230112: [2][128] S_t within a quarter
-constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136
+constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230112: [2][12] scale maxima per dequant warp
+constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136: tensor-memory address
+constexpr int kOffAbort = kOffTmem + 4;                                   // abort word (bounded waits)
 constexpr int kOffBar = kOffTmem + 16;                                    // 231152
 constexpr int kNumBars = 15;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231272
@@ -152,8 +172,7 @@ static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "opera
 
 constexpr uint32_t kBarSm = 1;     // named barrier of the softmax group
 constexpr uint32_t kBarAll = 2;    // dequant + softmax groups + MMA warp
-constexpr uint32_t kBarDq = 3;     // named barrier of the dequant group
-constexpr uint32_t kBarStq = 4;    // 4 + 4 * (tile parity) + lane quarter: S_t hand-off in a quarter
+constexpr uint32_t kBarDqTile = 3; // dequant group: the tile's scale maxima (once per tile)
 
 struct SplitParams {
   const uint8_t* kv;
@@ -163,6 +182,7 @@ struct SplitParams {
   Workspace ws;
   int B;
   unsigned long long timeout_ns;
+  int stall_producer;  // test hook: the producer issues no copy, so the first wait on a stage gives up
 };
 
 // ---- tile iterator: identical walk for every role of a CTA --------------------
@@ -394,12 +414,29 @@ __global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32
 }
 
 // ------------------------------------------------------------------------------
+// Bounded wait of the split kernel: gives up after p.timeout_ns of global time, raises
+// MLA_DEVICE_TIMEOUT in the status word and sets the CTA's abort word.  After that every
+// wait of the thread is a single test, so the CTA runs to its end without blocking: the
+// roles keep their control flow (every named barrier is still reached by all its warps),
+// and the producer and the MMA warp, which read the abort word once per tile, issue no
+// further asynchronous work and drain what they issued.
+// The abort word lives at a fixed offset of the dynamic shared memory; addressed through the
+// symbol, its address is a constant (no pointer kept live across the kernel).
+extern __shared__ __align__(1024) uint8_t dyn_smem[];
+__device__ __forceinline__ volatile int* abort_word() {
+  return reinterpret_cast<volatile int*>(dyn_smem + kOffAbort);
+}
+// The failure path, out of line (it runs at most once per thread).
+__device__ __noinline__ void flag_timeout(int* status) {
+  *abort_word() = 1;
+  atomicOr(status, kDeviceTimeout);
+}
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, const SplitParams& p,
                                              bool& aborted) {
   if (aborted) return mbar_try_wait(bar, parity);
   if (mbar_wait(bar, parity, p.timeout_ns)) return true;
   aborted = true;
-  atomicOr(&p.ws.meta[kMetaStatus], kDeviceTimeout);
+  flag_timeout(&p.ws.meta[kMetaStatus]);
   return false;
 }
 
@@ -421,74 +458,76 @@ __device__ __forceinline__ void chunk_to_e5m2(const uint4 w, uint32_t f2, uint32
   }
 }
 
-// K tile -> tensor memory as e5m2: K[t][d] = e2m1 * 2^(s_tb - S_t), exact for
-// s_tb >= S_t - 14; blocks further below the token's largest are zero (their elements
-// are under 2^-13 of the token's maximum).  Token t = this thread's lane of the
-// quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
+// Reference exponent of tile k: R_k = T_k, the largest scale byte of the tile, at a segment
+// start or when T_k exceeds the previous reference; the previous reference while T_k stays
+// within kRefSlack below it (no accumulator rescale for small steps down); never more than
+// kRefDrop below the largest reference of the segment so far, so that accumulated values
+// stay within fp32 range when they are expressed against a much lower reference.
+constexpr int kRefSlack = 4;
+constexpr int kRefDrop = 64;
+__device__ __forceinline__ int next_reference(int T, int r_prev, int r_max, bool seg_first) {
+  if (seg_first || T > r_prev) return T;
+  if (T < r_prev - kRefSlack) return max(T, r_max - kRefDrop);
+  return r_prev;
+}
+
+// K tile -> tensor memory as e5m2 against the tile reference R (one exponent for every token
+// of the tile): K[t][d] = e2m1 * 2^(s_tb - R + kHead).  R >= every scale byte of the tile, so
+// the largest possible element is 6 * 2^13, below the e5m2 maximum; a block is exact for
+// s_tb >= R - 27 (its fp16 factor 2^(s_tb - R + 13) is a normal number down to 2^-14, and every
+// product is then a normal or subnormal e5m2 value with a zero low byte in fp16); blocks
+// further below are zero.  Tokens past the tile are zero.  Token t = this thread's lane of
+// the quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
 // pair's bytes are loaded while this pair is converted; one 16-column store per pair).
-// Part 0 finds S_t, hands it to the quarter's other parts through stq and a named
-// barrier of the quarter's parts (which also orders every part's V^T copy of the
-// previous tile, read from this K buffer, before any part overwrites it), and stores
-// it in tensor-memory column st_col for the softmax group (0 for tokens past the tile).
-__device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, uint32_t a_lane,
-                                               uint32_t st_col, int* stq, uint32_t bar_id, int sc_mis) {
+// Every dequant warp first takes the largest scale byte of its blocks over its 32 tokens;
+// the twelve maxima meet in tq (this tile's parity) behind a barrier of the whole dequant
+// group, which also orders every part's V^T copy of the previous tile, read from the K
+// buffer about to be overwritten, before any part overwrites it.  Part 0 stores R in
+// tensor-memory column r_col for the softmax group.  Returns R.
+__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, int q4,
+                                              uint32_t a_lane, uint32_t r_col, int* tq, int sc_mis, int r_prev,
+                                              int r_max, bool seg_first) {
   const bool valid = t < n;
   const uint8_t* sb = st + kStagePackedBytes + (int)((sc_mis + (long long)t0 * kNScale) & 15) + t * kNScale;
-  int St = 0;
-  if (part == 0) {
-    if (valid) {
-      if ((smem_u32(sb) & 1u) == 0) {
-        // 18 bytes at an even address: nine 16-bit loads; the largest high byte is the
-        // high byte of the largest 16-bit word
-        uint32_t mhi = 0, mlo = 0;
-#pragma unroll
-        for (int i = 0; i < kNScale / 2; ++i) {
-          const uint32_t two = *reinterpret_cast<const uint16_t*>(sb + 2 * i);
-          mhi = max(mhi, two);
-          mlo = max(mlo, two & 0xFFu);
-        }
-        St = (int)max(mhi >> 8, mlo);
-      } else {  // odd address (kv_scale at an odd offset from a 16-byte boundary): byte loads
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < kNScale; ++i) m = max(m, (uint32_t)sb[i]);
-        St = (int)m;
-      }
-    }
-    stq[t] = St;
-    // a full barrier, not an arrive: the K buffer this part is about to overwrite held
-    // the previous tile, whose V^T the other parts may still be copying
-    named_sync(bar_id, 32 * kDqParts);
-    const uint32_t sv[1] = {(uint32_t)St};
-    tmem_st1(st_col, sv);
-  } else {
-    named_sync(bar_id, 32 * kDqParts);
-    St = stq[t];
-  }
   constexpr int kNb = kNScale / kDqParts;  // consecutive blocks b0 .. b0 + kNb - 1 of this part
   static_assert(kNScale % kDqParts == 0 && kNb % 2 == 0, "pairs of blocks per part");
   const int b0 = part * kNb;
-  const int sbias = valid ? 15 - St : -1024;  // f16 exponent field of 2^(s - S_t) is s + sbias when positive
-  const uint8_t* row = st + t * kPacked + 16 * b0;
   const uint8_t* sp = sb + b0;
+  int m = 0;
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < kNb; ++j) m = max(m, (int)sp[j]);
+  }
+  m = (int)__reduce_max_sync(0xffffffffu, (unsigned)m);
+  if ((t & 31) == 0) tq[part * 4 + q4] = m;
+  named_sync(kBarDqTile, kDqThreads);
+  int T = 0;
+#pragma unroll
+  for (int i = 0; i < kDqWarps; ++i) T = max(T, tq[i]);
+  const int R = next_reference(T, r_prev, r_max, seg_first);
+  if (part == 0) {
+    const uint32_t rv[1] = {(uint32_t)R};
+    tmem_st1(r_col, rv);
+  }
+  // f16 exponent field of 2^(s - R + kHead) is s + sbias when positive
+  const int sbias = valid ? 15 + kHead - R : -1024;
+  const uint8_t* row = st + t * kPacked + 16 * b0;
   uint4 wa = *reinterpret_cast<const uint4*>(row), wb = *reinterpret_cast<const uint4*>(row + 16);
-  int sa = sp[0], sc = sp[1];
   // not unrolled: the warp roles of a CTA share the instruction caches
 #pragma unroll 1
   for (int j = 0; j < kNb; j += 2) {
     const uint4 xa = wa, xb = wb;
-    const int ta = sa, tb = sc;
     if (j + 2 < kNb) {
       wa = *reinterpret_cast<const uint4*>(row + 16 * j + 32);
       wb = *reinterpret_cast<const uint4*>(row + 16 * j + 48);
-      sa = sp[j + 2];
-      sc = sp[j + 3];
     }
+    const int ta = sp[j], tb = sp[j + 1];
     uint32_t e[16];
     chunk_to_e5m2(xa, (uint32_t)max(ta + sbias, 0) * 0x04000400u, *reinterpret_cast<uint32_t(*)[8]>(&e[0]));
     chunk_to_e5m2(xb, (uint32_t)max(tb + sbias, 0) * 0x04000400u, *reinterpret_cast<uint32_t(*)[8]>(&e[8]));
     tmem_st16(a_lane + 8 * (b0 + j), e);
   }
+  return R;
 }
 
 // Maximum (kMax) or sum over the 32 lanes of sixteen per-lane values; lane L ends
@@ -526,7 +565,7 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* smem = dyn_smem;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
@@ -538,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bar_kready = bars + 8;    // [2] K tile in tensor-memory buffer b ready, its Qhat landed (dequant group)
   uint64_t* bar_vready = bars + 10;   // V^T of a tile in shared memory (dequant group)
   uint64_t* bar_pready = bars + 11;   // P^T and any O^T rescale of a tile done (softmax group)
-  uint64_t* bar_qk = bars + 12;       // [2] S^T buffer b and the tile's S_t written (MMA commit)
+  uint64_t* bar_qk = bars + 12;       // [2] S^T buffer b written (MMA commit); its tile's R_k is in tensor memory
   uint64_t* bar_pv = bars + 14;       // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -557,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     fence_barrier_init();
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+  if (tid == 0) *abort_word() = 0;
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   // Everything above overlaps the partition kernel (programmatic dependent launch); its
   // results are read from here on.  The merge kernel may be scheduled from now on: it waits
@@ -585,12 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     const long long scale_end16 = scale_end & ~15LL;
     const long long head16 = (p.sc_mis + 15) & ~15LL;
     int k = 0;
-    do {
+    if (!p.stall_producer) do {
       const int s = k % kStages;
-      if (k >= kStages) wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted);
+      if (k >= kStages && !wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted)) break;
       const int j = it.seg;
       // segment j's Qhat goes to buffer j & 1 once the last QK^T of segment j - 2 read it
-      if (it.first && j >= 2) wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted);
+      if (it.first && j >= 2 && !wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted))
+        break;
       uint8_t* st = smem + kOffStages + s * kStageBytes;
       // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
       // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
@@ -612,7 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
                  &bar_full[s], pol_q);
       ++k;
-    } while (it.next());
+    } while (!*abort_word() && it.next());
+    // Drain before this warp leaves: the last phase issued on each stage completes once its
+    // copies have landed (in a normal run the dequant group has waited for all of them; after
+    // an abort it may not have, and no copy may still be writing when the CTA exits).
+    for (int s = 0; s < kStages && s < k; ++s) {
+      const int kl = s + ((k - 1 - s) / kStages) * kStages;  // last tile issued on stage s
+      mbar_wait(&bar_full[s], (uint32_t)(kl / kStages) & 1u, p.timeout_ns);
+    }
     return;
   }
 
@@ -621,19 +669,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   // once its V^T and P^T are ready.
   if (warp == kMmaWarp) {
     const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
-    const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, true, true);
+    const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE5M2, true, true);
     const uint64_t dq0 = smem_desc_kmajor(smem_u32(smem + kOffQhat), kQLbo, kQSbo);
     const uint64_t dv0 = smem_desc_mnmajor(smem_u32(smem + kOffVt), kVtLbo, kVtSbo);
     const uint64_t dp0 = smem_desc_mnmajor(smem_u32(smem + kOffPt), kPtLbo, kPtSbo);
     TileIter cur = it, nxt = it;
     bool has_next = nxt.next();
     int k = 0;
+    // the last commit issued: it arrives once every MMA issued before it has completed
+    uint64_t* last_bar = nullptr;
+    uint32_t last_par = 0;
     for (int kk = 0;; ++kk) {
+      if (*abort_word()) break;  // another role gave up: issue nothing more
       // QK^T of tile kk (kk = 0 before the loop proper, then kk = k + 1)
       if (kk == 0 || has_next) {
         const int q = kk;
         const TileIter& qt = kk == 0 ? cur : nxt;
-        wait_or_flag(&bar_kready[q & 1], (q >> 1) & 1, p, aborted);
+        if (!wait_or_flag(&bar_kready[q & 1], (q >> 1) & 1, p, aborted)) break;
         tc_fence_after();
         const uint32_t bq = q & 1;
         const uint64_t dq = dq0 + (uint64_t)(((qt.seg & 1) * kQhatBytes) >> 4);
@@ -642,12 +694,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           umma_f8_ts_warp(tmem + kColS + 32 * bq, tmem + kColA + kColsA * bq + 8 * ks,
                           dq + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
         umma_commit_warp(&bar_qk[bq]);
-        if (qt.last) umma_commit_warp(&bar_qfree[qt.seg & 1]);  // the segment's Qhat buffer may be refilled
+        last_bar = &bar_qk[bq];
+        last_par = (uint32_t)(q >> 1) & 1u;
+        if (qt.last) {  // the segment's Qhat buffer may be refilled
+          umma_commit_warp(&bar_qfree[qt.seg & 1]);
+          last_bar = &bar_qfree[qt.seg & 1];
+          last_par = (uint32_t)(qt.seg >> 1) & 1u;
+        }
       }
       if (kk == 0) continue;
       // P.V of tile k
-      wait_or_flag(bar_vready, k & 1, p, aborted);
-      wait_or_flag(bar_pready, k & 1, p, aborted);
+      if (!wait_or_flag(bar_vready, k & 1, p, aborted)) break;
+      if (!wait_or_flag(bar_pready, k & 1, p, aborted)) break;
       tc_fence_after();
       const uint64_t dp = dp0 + (uint64_t)(((k & 1) * kPtBytes) >> 4);
       const bool seg_first = cur.first;
@@ -658,14 +716,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           umma_f8_ss_warp(tmem + kColO + 32 * blk, dv0 + (uint64_t)((blk * kVtBlock + js * 4 * kVtLbo) >> 4),
                           dp + (uint64_t)((js * 4 * kPtLbo) >> 4), idesc_pv, (js > 0 || !seg_first) ? 1u : 0u);
       umma_commit_warp(bar_pv);
+      last_bar = bar_pv;
+      last_par = (uint32_t)k & 1u;
       if (!has_next) break;
       cur = nxt;
       has_next = nxt.next();
       ++k;
     }
-    // every P.V completed (the softmax group waited for each segment's last one) and
-    // the other groups are done with tensor memory: release it (the allocating warp)
+    // The other groups are done with tensor memory, and every MMA has completed: in a normal
+    // run the softmax group waited for each segment's last P.V; after an abort the last
+    // commit is waited for here (MMAs complete on their own).  Then release tensor memory
+    // (the allocating warp).
     named_sync(kBarAll, kTokThreads + 32);
+    if (last_bar) mbar_wait(last_bar, last_par, p.timeout_ns);
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
     return;
@@ -691,9 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     // prologue: tile 0 (a segment start)
     if (gtid < kHeads) chs[(it.seg & 3) * kHeads + gtid] = p.ws.qch[it.b * kHeads + gtid];
     wait_or_flag(&bar_full[0], 0, p, aborted);
-    int* stq = reinterpret_cast<int*>(smem + kOffStq);  // [2][128]
-    k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, t_lane + kColA, t_lane + kColSt, stq, kBarStq + q4,
-                   p.sc_mis);
+    int* tq = reinterpret_cast<int*>(smem + kOffStq);  // [2 tile parities][12 dequant warps]
+    // reference exponent of the last converted tile and the largest of its segment
+    int r_ref = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, q4, t_lane + kColA, t_lane + kColSt, tq,
+                               p.sc_mis, 0, 0, true);
+    int r_max = r_ref;
     tc_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -716,11 +781,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         if (k == 1) wait_or_flag(&bar_qk[0], 0, p, aborted);
         if (new_seg) chs[(it.seg & 3) * kHeads + gtid] = chv;
         tc_fence_after();
-        // S_t of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3, which
-        // finished before P.V of tile k-3 (waited for two iterations ago)
-        k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.t0, it.n, t, part,
-                       t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
-                       stq + ((k + 1) & 1) * kTile, kBarStq + 4 * ((k + 1) & 1) + q4, p.sc_mis);
+        // the reference of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3,
+        // which finished before P.V of tile k-3 (waited for two iterations ago)
+        r_ref = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.t0, it.n, t, part, q4,
+                               t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
+                               tq + ((k + 1) & 1) * kDqWarps, p.sc_mis, r_ref, r_max, it.first);
+        r_max = it.first ? r_ref : max(r_max, r_ref);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -779,15 +845,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       const bool valid = t < it.n;
       const bool seg_first = it.first;
       const float* ch = chs + (it.seg & 3) * kHeads;
-      // S^T and the tile's token exponents S_t (stored by the dequant group before the K tile
-      // that QK^T read was declared ready)
+      // S^T and the tile's reference exponent R_k (stored by the dequant group before the K
+      // tile that QK^T read was declared ready; the same value in every lane)
       wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
       tc_fence_after();
-      int St;
-      float stok;
+      int Rk;
       float s2[16];
       float* hmax = reinterpret_cast<float*>(smem + kOffHmax) + (k & 1) * 4 * kHeads;  // [16 heads][4 quarters]
-      int* rwb = reinterpret_cast<int*>(smem + kOffRw) + (k & 1) * 4;
       {
         uint32_t rh[16], rl[16], sv[1];
         const uint32_t scol = t_lane + kColS + 32 * (k & 1);
@@ -795,9 +859,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         tmem_ld16_nowait(scol + 16, rl);
         tmem_ld1_nowait(t_lane + kColSt + (k & 3), sv);
         tc_wait_ld();
-        St = valid ? (int)sv[0] : 0;
-        stok = !valid ? 0.f : (St == 255 ? __int_as_float(0x7FC00000) : exp2i(St - 127));
-        // s = (hi + lo part scores) * (head factor * token factor); -inf past the tile's tokens
+        Rk = (int)sv[0];
+        // 2^(R_k - 127 - kHead): a power of two (also where it is subnormal), so the products
+        // below round only once; a tile holding a NaN scale byte (R_k = 255) gives NaN scores
+        const float stok = Rk == 255 ? __int_as_float(0x7FC00000) : exp2i(Rk - 127 - kHead);
+        // s = (hi + lo part scores) * (head factor * tile factor); -inf past the tile's tokens
+        // (their K rows are zero)
         const float2 st2 = make_float2(stok, stok);
         const float pen = valid ? 0.f : -INFINITY;
         const float2 pen2 = make_float2(pen, pen);
@@ -816,10 +883,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         }
       }
       // d = s - m with the running maxima as they stand.  When every score of the tile is
-      // within kMaxThresh of its head's maximum and every token exponent within kMaxThresh
-      // of R (one AND-reducing barrier over the group), nothing moves: no tile maxima are
-      // exchanged and P uses d as it is.  A moving maximum or a segment start takes the
-      // full path (the same decisions either way).
+      // within kMaxThresh of its head's maximum (one AND-reducing barrier over the group) and
+      // the tile's reference equals the previous one, nothing moves: no tile maxima are
+      // exchanged and P uses d as it is.  A moving maximum, a new reference or a segment
+      // start takes the full path (the same decisions either way).
       float d[16], alpha_v[16];
       float dmax = -INFINITY;
 #pragma unroll
@@ -831,33 +898,29 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         dmax = fmaxf(dmax, fmaxf(fmaxf(d0.x, d0.y), fmaxf(d1.x, d1.y)));
         alpha_v[i] = alpha_v[i + 1] = alpha_v[i + 2] = alpha_v[i + 3] = 1.f;
       }
-      const bool fits = !seg_first && dmax <= (float)kMaxThresh && (!valid || St <= R + kMaxThresh);
-      int Rnew = R;
+      const int Rnew = Rk;
+      const bool fits = !seg_first && dmax <= (float)(kMaxThresh + kPExp) && Rnew == R;
       bool resc = false;
       if (!named_sync_and(kBarSm, kSmThreads, fits)) {
         // tile maxima: per head over the warp's tokens, then over the four warps
         const float wm = warp_reduce16<true>(s2, lane);
         if ((lane & 1) == 0) hmax[(lane >> 1) * 4 + q4] = wm;
-        const int rw = __reduce_max_sync(0xffffffffu, valid ? St : 0);
-        if (lane == 0) rwb[q4] = rw;
         named_sync(kBarSm, kSmThreads);
         // running statistics: lane L computes head L >> 1; the lane pair agrees
         {
-          const int4 rwv = *reinterpret_cast<const int4*>(rwb);
-          const int Rtile = max(max(rwv.x, rwv.y), max(rwv.z, rwv.w));
-          Rnew = seg_first ? Rtile : (Rtile > R + kMaxThresh ? Rtile : R);
           const int h = lane >> 1;
           const float4 hm = *reinterpret_cast<const float4*>(hmax + h * 4);
           const float M = fmaxf(fmaxf(hm.x, hm.y), fmaxf(hm.z, hm.w));
           const float mo = mstate[h];
           float mn = mo, alpha = 1.f;
           bool moved = false;
+          // mstate holds m - kPExp (see kPExp)
           if (seg_first) {
-            mn = M;
+            mn = M - (float)kPExp;
             alpha = 0.f;
-          } else if (M > mo + (float)kMaxThresh) {
-            mn = M;
-            alpha = ex2(mo - M);
+          } else if (M > mo + (float)(kPExp + kMaxThresh)) {
+            mn = M - (float)kPExp;
+            alpha = ex2(mo - mn);
             moved = true;
           }
           resc = __any_sync(0xffffffffu, moved) || (!seg_first && Rnew != R);
@@ -878,8 +941,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           alpha_v[i] = b.x; alpha_v[i + 1] = b.y; alpha_v[i + 2] = b.z; alpha_v[i + 3] = b.w;
         }
       }
-      const float ptok = valid ? exp2i(St - Rnew) : 0.f;
-      const float2 ptok2 = make_float2(ptok, ptok);
       uint32_t phi[4], plo[4];
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
@@ -888,16 +949,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         const float2 ln = seg_first ? pv : f2fma(lp, make_float2(alpha_v[i], alpha_v[i + 1]), pv);
         l_part[i] = ln.x;
         l_part[i + 1] = ln.y;
-        const float2 pp = f2mul(pv, ptok2);
-        // P = hi + lo, both e4m3, split in f16 (P <= 2^8: the f16 rounding is 2^-11 relative and
-        // pp16 - hi is exact in f16)
-        const __half2 p16 = __floats2half2_rn(pp.x, pp.y);
+        // P' = hi + lo, both e5m2 (see kPExp); P' - hi is exact in f16
+        const __half2 p16 = __floats2half2_rn(pv.x, pv.y);
         const __nv_fp8x2_storage_t hi2 =
-            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&p16), __NV_SATFINITE, __NV_E4M3);
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3);
+            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&p16), __NV_SATFINITE, __NV_E5M2);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E5M2);
         const __half2 rest = __hsub2(p16, *reinterpret_cast<const __half2*>(&hr));
         const __nv_fp8x2_storage_t lo2 =
-            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rest), __NV_SATFINITE, __NV_E4M3);
+            __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rest), __NV_SATFINITE, __NV_E5M2);
         if ((i & 2) == 0) {
           phi[i >> 2] = (uint32_t)hi2;
           plo[i >> 2] = (uint32_t)lo2;
@@ -938,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pready);
       if (it.last) {
-        // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^(R-127) / l ----
+        // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^-kHead * 2^(R-127) / l ----
         float* lw = reinterpret_cast<float*>(smem + kOffLw);      // [16 heads][4 quarters]
         float* ofac = reinterpret_cast<float*>(smem + kOffMlast);  // [16] 2^(R-127) / l
         const float ls = warp_reduce16<false>(l_part, lane);
@@ -975,11 +1034,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
             __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
 #pragma unroll
             for (int h = 0; h < kHeads; ++h)
-              o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h]);
+              o[h * kDv] =
+                  __float2bfloat16_rn(((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h]);
           } else {
             float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
 #pragma unroll
-            for (int h = 0; h < kHeads; ++h) o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h];
+            for (int h = 0; h < kHeads; ++h)
+              o[h * kDv] = ((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h];
           }
         }
         tc_fence_before();

@@ -90,6 +90,16 @@ __device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t count, bool
       : "memory");
   return r != 0;
 }
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %3, 0;\n bar.red.or.pred p, %1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -164,15 +174,6 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lb
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version for this architecture
   return d;
-}
-// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// kind::f8f6f4 (fp8 e4m3 A and B, fp32 accumulate), both operands MN-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_mn_f32(int m, int n) {
-  return (1u << 4) | (1u << 15) | (1u << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 // Same layout rule as smem_desc_kmajor for MN-major operands: lbo = stride between
 // 8-row groups along K, sbo = stride between 16-byte chunks along M/N.

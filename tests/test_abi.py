@@ -19,7 +19,8 @@ def test_exports_every_declared_symbol(L):
     names = _lib.declared_functions()
     assert set(names) >= {"mla_decode_mxfp4", "mla_decode_mxfp4_ws", "mla_decode_mxfp4_workspace_bytes",
                           "mla_decode_mxfp4_device_status", "mla_decode_mxfp4_release", "mla_status_string",
-                          "mla_decode_mxfp4_ws_timed"}
+                          "mla_decode_mxfp4_ws_timed", "mla_decode_mxfp4_ws_stalled",
+                          "mla_decode_mxfp4_noalloc", "mla_decode_mxfp4_last_device_status"}
     for n in names:
         assert hasattr(L, n), n
 
@@ -41,6 +42,10 @@ def test_host_argument_checks(L):
     w = _lib.mla_decode_mxfp4_ws
     assert w(ok["q"], ok["kv"], ok["sc"], ok["ip"], ok["out"], 2, 1.0, None, 0, 1 << 20) == _lib.MLA_ERR_NULL_PTR
     assert w(ok["q"], ok["kv"], ok["sc"], ok["ip"], ok["out"], 2, 1.0, None, 0x10010, 1 << 20) == _lib.MLA_ERR_BAD_ALIGN
+    st = _lib.mla_decode_mxfp4_ws_stalled  # the test hook's wait limit must be 1 ns .. 1 s
+    for bad in (0, 1_000_000_001):
+        assert st(ok["q"], ok["kv"], ok["sc"], ok["ip"], ok["out"], 2, 1.0, None, 0x10000, 1 << 20,
+                  bad) == _lib.MLA_ERR_BAD_SCALE
 
 
 def test_status_strings(L):
