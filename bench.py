@@ -318,6 +318,100 @@ class DeviceWorkload:
                 "traffic": _traffic_per_launch(workload)}
 
 
+class GeneralWorkload(DeviceWorkload):
+    """A further layout of a workload, timed through its own C entry point: the KV cache as fp8
+    with a per-tensor scale ("fp8"), in scattered pages of 64 rows ("paged64"), or with two
+    query rows per sequence ("q2")."""
+
+    def __init__(self, name, dev, stream):
+        import torch
+
+        import mla_inputs as MI
+        from mla_decode_attention_mxfp4_gb300 import _lib, alloc_workspace
+        base, form = name.split(":")
+        self.name, self.form, self.dev, self.stream, self._lib = name, form, dev, stream, _lib
+        if form == "fp8":
+            d = MI.make_fp8_inputs(base)
+            self.d = d
+            self.nbytes = d.algorithmic_bytes()
+            self.split_bytes = d.total_kv * 576 + d.q.shape[0] * 18432
+            self.in_bytes = d.q.numel() * 2 + d.kv_fp8.numel()
+            self.total_q = d.batch
+            tensors = lambda: (d.q.to(dev), d.kv_fp8.to(dev), torch.tensor([d.kv_scale], dtype=torch.float32,
+                                                                              device=dev), d.kv_indptr.to(dev))
+        else:
+            d = MI.make_inputs(base)
+            self.d = d
+            if form == "paged64":
+                kp, ks, ip, ix, last, npages = MI.scatter_into_pages(d, 64, seed=40, spare_pages=0)
+                self.paged = (ix, last, npages)
+                tensors = lambda: (d.q.to(dev), kp.to(dev), ks.to(dev), ip.to(dev), ix.to(dev), last.to(dev))
+                self.total_q = d.batch
+                q_bytes = d.q.numel() * 2
+            elif form == "q2":
+                q, qo = MI.query_rows([2] * d.batch, seed=41)
+                self.qo = qo
+                tensors = lambda: (q.to(dev), d.kv_packed.to(dev), d.kv_scale.to(dev), d.kv_indptr.to(dev),
+                                   qo.to(dev))
+                self.total_q = int(qo[-1])
+                q_bytes = q.numel() * 2
+            else:
+                raise ValueError(name)
+            kv_bytes = d.kv_packed.numel() + d.kv_scale.numel()
+            self.nbytes = q_bytes + kv_bytes + self.total_q * 16 * 512 * 2
+            # each query row reads its sequence's KV rows once
+            rows_read = d.total_kv * (2 if form == "q2" else 1)
+            self.split_bytes = rows_read * 306 + self.total_q * 18432
+            self.in_bytes = q_bytes + kv_bytes
+        self.copies = max(2, min(8, math.ceil(4 * L2_BYTES / self.in_bytes)))
+        self.bufs = []
+        for _ in range(self.copies):
+            self.bufs.append(tensors() + (torch.empty(self.total_q, 16, 512, dtype=torch.bfloat16, device=dev),))
+        self.ws = alloc_workspace(max(self.d.batch, self.total_q), dev)
+        torch.cuda.synchronize(dev)
+
+    def call(self, i, ev_b=None, ev_e=None):
+        b = self.bufs[i % self.copies]
+        L, d = self._lib, self.d
+        if self.form == "fp8":
+            q, kv, sc, ip, out = b
+            rc = L.mla_decode_fp8_ws_timed(q.data_ptr(), kv.data_ptr(), sc.data_ptr(), None, ip.data_ptr(),
+                                           kv.shape[0], out.data_ptr(), d.batch, d.batch, d.sm_scale,
+                                           self.stream.cuda_stream, self.ws.data_ptr(), self.ws.numel(), ev_b, ev_e)
+        elif self.form == "paged64":
+            q, kp, ks, ip, ix, last, out = b
+            rc = L.mla_decode_mxfp4_paged_ws_timed(q.data_ptr(), kp.data_ptr(), ks.data_ptr(), None, ip.data_ptr(),
+                                                   ix.data_ptr(), last.data_ptr(), 64, self.paged[2], out.data_ptr(),
+                                                   d.batch, d.batch, d.sm_scale, self.stream.cuda_stream,
+                                                   self.ws.data_ptr(), self.ws.numel(), ev_b, ev_e)
+        else:
+            q, kv, sc, ip, qo, out = b
+            rc = L.mla_decode_mxfp4_paged_ws_timed(q.data_ptr(), kv.data_ptr(), sc.data_ptr(), qo.data_ptr(),
+                                                   ip.data_ptr(), None, None, 0, 0, out.data_ptr(), d.batch,
+                                                   self.total_q, d.sm_scale, self.stream.cuda_stream,
+                                                   self.ws.data_ptr(), self.ws.numel(), ev_b, ev_e)
+        if rc != 0:
+            raise RuntimeError(L.status_string(rc))
+
+    def config(self):
+        import mla_inputs as MI
+        base = self.name.split(":")[0]
+        w = MI.WORKLOADS[base]
+        desc = {"workload": f"{self.name}: {w.note}", "batch": self.d.batch, "query_rows": self.total_q,
+                "tokens": self.d.total_kv, "bytes_per_call": self.nbytes,
+                "kv_format": {"fp8": "fp8 e4m3, one per-tensor scale (576 B per token)",
+                              "paged64": "MXFP4 in scattered pages of 64 rows",
+                              "q2": "MXFP4, two query rows per sequence (each row reads its sequence's KV)"}[self.form],
+                "l2": self.l2_note()}
+        return desc
+
+    def roofline(self, split_ms, peak, peak_src, workload):
+        r = DeviceWorkload.roofline(self, split_ms, peak, peak_src, workload)
+        r["kernel"] = "mla_split_fp8_kernel" if self.form == "fp8" else "mla_split_kernel"
+        r["traffic"] = None
+        return r
+
+
 NUMERICS = ("K/V as e5m2 (exact e2m1*2^k per token, 13 binades of headroom), query and P as two e4m3 "
             "terms each, tcgen05 f8f6f4 MMAs with fp32 accumulation, fp32 softmax and merge, bf16 out")
 
@@ -417,6 +511,20 @@ def run_native(args):
     for name in args.extra:
         if name == args.workload:
             continue
+        if ":" in name:
+            X = GeneralWorkload(name, dev, stream)
+            with torch.cuda.stream(stream):
+                for i in range(max(args.warmup, 10)):
+                    X.call(i)
+                xs = max(args.steps, 20)
+                xms = X.time_calls(xs)
+                xsplit = X.time_split_kernel(xs)
+            extra[name] = {"config": X.config(), "value": whole_job_gbps(ws, X.nbytes, xms), "unit": "GB/s",
+                           "us_per_call": xms * 1e3, "frac_of_hbm_peak": X.nbytes / (xms * 1e-3) / 1e9 / peak,
+                           "steps": xs, "roofline": X.roofline(xsplit, peak, peak_src, name)}
+            del X
+            torch.cuda.empty_cache()
+            continue
         dx = MI.make_inputs(name)
         X = DeviceWorkload(dx, dev, stream)
         with torch.cuda.stream(stream):
@@ -472,7 +580,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="uniform")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--extra", nargs="*", default=["ragged"],
+    ap.add_argument("--extra", nargs="*",
+                    default=["ragged", "uniform:fp8", "ragged:fp8", "ragged:paged64", "uniform:q2"],
                     help="further workloads measured on the device and reported under extra_workloads")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -64,7 +64,10 @@ enum mla_status {
   MLA_ERR_BAD_SCALE = 4,  /* sm_scale is not finite                                */
   MLA_ERR_WORKSPACE = 5,  /* workspace too small, or would have to grow during
                              stream capture                                        */
-  MLA_ERR_CUDA = 6        /* a CUDA runtime call or kernel launch failed           */
+  MLA_ERR_CUDA = 6,       /* a CUDA runtime call or kernel launch failed           */
+  MLA_ERR_BAD_LAYOUT = 7  /* mla_decode_mxfp4_paged_ws: total_q != batch without
+                             qo_indptr, page_size < 1, num_pages < 0, or
+                             kv_last_page_len missing with kv_indices             */
 };
 
 /* Bits of the device status word (OR-ed; cleared at the start of every call). */
@@ -108,6 +111,78 @@ int mla_decode_mxfp4_ws_timed(const void* q, const uint8_t* kv_packed, const uin
                               const int32_t* kv_indptr, void* out, int batch, float sm_scale,
                               mla_stream_t stream, void* workspace, size_t ws_bytes,
                               void* ev_split_begin, void* ev_split_end);
+
+/*
+ * General layouts: several query rows per sequence and/or paged KV.
+ *
+ * Several query rows per sequence (MTP / speculative decode; kernelindex amd-mixed-mla
+ * 676098 "_naive_fallback" and 608791 "_build_decode_metadata"'s qo_indptr): with qo_indptr
+ * non-NULL, query rows [qo_indptr[b], qo_indptr[b+1]) of sequence b each attend, with no
+ * mask, to all of sequence b's KV rows; q is bf16 [total_q][16][576] and out bf16
+ * [total_q][16][512] (a row outside every sequence's range gives zeros).  With qo_indptr
+ * NULL, total_q must equal batch and row b is sequence b's single query.
+ *
+ * Paged KV (676098 "_aiter_mla_decode": kv_indptr over kv_indices, kv_last_page_len): with
+ * kv_indices non-NULL, kv_indptr[b]..kv_indptr[b+1] index kv_indices, whose entries are page
+ * ids in [0, num_pages); page p holds physical rows [p*page_size, (p+1)*page_size) of
+ * kv_packed and kv_scale (so both buffers hold num_pages*page_size rows), and sequence b's
+ * KV rows are, in order, its pages' rows, all page_size of them except kv_last_page_len[b]
+ * (1..page_size) of its last page.  A sequence with no pages is empty.  page_size may be any
+ * positive value; multiples of 8 keep the scale rows of every page 16-byte congruent, so
+ * they are bulk-copied (other sizes are read with plain loads: correct, slower).  With
+ * kv_indices NULL, kv_indptr counts rows as in mla_decode_mxfp4 (page_size, num_pages and
+ * kv_last_page_len are ignored).
+ *
+ * Out-of-range page ids are clamped into the buffers and raise MLA_DEVICE_BAD_INDPTR, as do
+ * malformed kv_indptr / qo_indptr (clamped to non-decreasing sequences within their ranges)
+ * and kv_last_page_len outside 1..page_size (clamped).  The workspace must hold at least
+ * mla_decode_mxfp4_workspace_bytes(max(batch, total_q), device) bytes, 256-byte aligned; the
+ * other arguments, layouts and errors are those of mla_decode_mxfp4_ws.  The _timed variant
+ * records `ev_split_begin` / `ev_split_end` (either may be NULL) around the attention kernel,
+ * as mla_decode_mxfp4_ws_timed does.
+ */
+int mla_decode_mxfp4_paged_ws(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                              const int32_t* qo_indptr, const int32_t* kv_indptr,
+                              const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                              int page_size, int num_pages, void* out, int batch, int total_q,
+                              float sm_scale, mla_stream_t stream, void* workspace, size_t ws_bytes);
+int mla_decode_mxfp4_paged_ws_timed(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale,
+                                    const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                    const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                                    int page_size, int num_pages, void* out, int batch, int total_q,
+                                    float sm_scale, mla_stream_t stream, void* workspace,
+                                    size_t ws_bytes, void* ev_split_begin, void* ev_split_end);
+
+/*
+ * fp8 KV with one per-tensor scale (the pages' production path: kernelindex amd-mixed-mla
+ * 676098 "_aiter_mla_decode", 717900 "_decode"):
+ *
+ *   K[t][d] = e4m3(kv_fp8[t][d]) * (*kv_scale),  d < 576;   V[t][d] = K[t][d],  d < 512
+ *   out[r][h][:] = sum_t softmax_t(sm_scale * q[r][h] . K[t]) V[t]
+ *
+ * over sequence b's rows [kv_indptr[b], kv_indptr[b+1]) for each of its query rows r (one per
+ * sequence with qo_indptr NULL, total_q == batch; else rows [qo_indptr[b], qo_indptr[b+1]) as
+ * for mla_decode_mxfp4_paged_ws).  e4m3 is the OCP "fn" encoding (no infinities; 0x7F/0xFF
+ * are NaN).  The query is used as given (bf16).
+ *
+ * Layouts: q bf16 [total_q][16][576] (16-byte aligned); kv_fp8 uint8 [kv_rows][576] (16-byte
+ * aligned; kv_rows > 0 is the number of rows the buffer holds: kv_indptr is clamped to it,
+ * raising MLA_DEVICE_BAD_INDPTR, so no row outside the buffer is read); kv_scale a DEVICE
+ * pointer to one float (read by the kernel, so it may change between calls, or inside a
+ * captured graph, without the host reading it); kv_indptr int32 [batch+1]; out bf16
+ * [total_q][16][512].  Workspace: at least mla_decode_mxfp4_workspace_bytes(max(batch,
+ * total_q), device) bytes, 256-byte aligned.  Errors as mla_decode_mxfp4_paged_ws.  The _timed
+ * variant records events around the attention kernel.
+ */
+int mla_decode_fp8_ws(const void* q, const uint8_t* kv_fp8, const float* kv_scale,
+                      const int32_t* qo_indptr, const int32_t* kv_indptr, int kv_rows, void* out,
+                      int batch, int total_q, float sm_scale, mla_stream_t stream, void* workspace,
+                      size_t ws_bytes);
+int mla_decode_fp8_ws_timed(const void* q, const uint8_t* kv_fp8, const float* kv_scale,
+                            const int32_t* qo_indptr, const int32_t* kv_indptr, int kv_rows,
+                            void* out, int batch, int total_q, float sm_scale, mla_stream_t stream,
+                            void* workspace, size_t ws_bytes, void* ev_split_begin,
+                            void* ev_split_end);
 
 /* Test-only variant of mla_decode_mxfp4_ws that exercises the failure path of the
  * attention kernel's bounded waits without faulting anything: the kernel's copy

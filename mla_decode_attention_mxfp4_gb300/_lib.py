@@ -22,6 +22,7 @@ MLA_ERR_BAD_ALIGN = 3
 MLA_ERR_BAD_SCALE = 4
 MLA_ERR_WORKSPACE = 5
 MLA_ERR_CUDA = 6
+MLA_ERR_BAD_LAYOUT = 7
 MLA_DEVICE_BAD_INDPTR = 1
 MLA_DEVICE_TIMEOUT = 2
 # mla_decode_mxfp4_device_status(stream, MLA_STATIC_SCRATCH, ...) reads the no-allocation scratch
@@ -61,6 +62,14 @@ def lib():
     L.mla_decode_mxfp4_ws.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz]
     L.mla_decode_mxfp4_ws_timed.restype = i
     L.mla_decode_mxfp4_ws_timed.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz, vp, vp]
+    L.mla_decode_mxfp4_paged_ws.restype = i
+    L.mla_decode_mxfp4_paged_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, vp, i, i, f, vp, vp, sz]
+    L.mla_decode_mxfp4_paged_ws_timed.restype = i
+    L.mla_decode_mxfp4_paged_ws_timed.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, vp, i, i, f, vp, vp, sz, vp, vp]
+    L.mla_decode_fp8_ws.restype = i
+    L.mla_decode_fp8_ws.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, f, vp, vp, sz]
+    L.mla_decode_fp8_ws_timed.restype = i
+    L.mla_decode_fp8_ws_timed.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, f, vp, vp, sz, vp, vp]
     L.mla_decode_mxfp4_ws_stalled.restype = i
     L.mla_decode_mxfp4_ws_stalled.argtypes = [vp, vp, vp, vp, vp, i, f, vp, vp, sz, ctypes.c_ulonglong]
     L.mla_decode_mxfp4_workspace_bytes.restype = sz
@@ -97,6 +106,35 @@ def mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_
                               ws_bytes, ev_split_begin, ev_split_end) -> int:
     return lib().mla_decode_mxfp4_ws_timed(q, kv_packed, kv_scale, kv_indptr, out, int(batch), float(sm_scale),
                                            stream, workspace, int(ws_bytes), ev_split_begin, ev_split_end)
+
+
+def mla_decode_mxfp4_paged_ws(q, kv_packed, kv_scale, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, page_size,
+                              num_pages, out, batch, total_q, sm_scale, stream, workspace, ws_bytes) -> int:
+    return lib().mla_decode_mxfp4_paged_ws(q, kv_packed, kv_scale, qo_indptr, kv_indptr, kv_indices, kv_last_page_len,
+                                           int(page_size), int(num_pages), out, int(batch), int(total_q),
+                                           float(sm_scale), stream, workspace, int(ws_bytes))
+
+
+def mla_decode_mxfp4_paged_ws_timed(q, kv_packed, kv_scale, qo_indptr, kv_indptr, kv_indices, kv_last_page_len,
+                                    page_size, num_pages, out, batch, total_q, sm_scale, stream, workspace, ws_bytes,
+                                    ev_split_begin, ev_split_end) -> int:
+    return lib().mla_decode_mxfp4_paged_ws_timed(q, kv_packed, kv_scale, qo_indptr, kv_indptr, kv_indices,
+                                                 kv_last_page_len, int(page_size), int(num_pages), out, int(batch),
+                                                 int(total_q), float(sm_scale), stream, workspace, int(ws_bytes),
+                                                 ev_split_begin, ev_split_end)
+
+
+def mla_decode_fp8_ws(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, kv_rows, out, batch, total_q, sm_scale, stream,
+                      workspace, ws_bytes) -> int:
+    return lib().mla_decode_fp8_ws(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, int(kv_rows), out, int(batch),
+                                   int(total_q), float(sm_scale), stream, workspace, int(ws_bytes))
+
+
+def mla_decode_fp8_ws_timed(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, kv_rows, out, batch, total_q, sm_scale,
+                            stream, workspace, ws_bytes, ev_split_begin, ev_split_end) -> int:
+    return lib().mla_decode_fp8_ws_timed(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, int(kv_rows), out, int(batch),
+                                         int(total_q), float(sm_scale), stream, workspace, int(ws_bytes),
+                                         ev_split_begin, ev_split_end)
 
 
 def mla_decode_mxfp4_ws_stalled(q, kv_packed, kv_scale, kv_indptr, out, batch, sm_scale, stream, workspace,

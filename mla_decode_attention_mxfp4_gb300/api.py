@@ -79,6 +79,79 @@ def decode(q: torch.Tensor, kv_packed: torch.Tensor, kv_scale: torch.Tensor, kv_
     return out
 
 
+def decode_general(q: torch.Tensor, kv_packed: torch.Tensor, kv_scale: torch.Tensor, kv_indptr: torch.Tensor,
+                   sm_scale: float, qo_indptr: torch.Tensor | None = None, kv_indices: torch.Tensor | None = None,
+                   kv_last_page_len: torch.Tensor | None = None, page_size: int = 0, num_pages: int = 0,
+                   out: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None,
+                   workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode with several query rows per sequence (qo_indptr) and/or paged KV (kv_indices,
+    kv_last_page_len, page_size, num_pages); see mla_decode_mxfp4_paged_ws.  q is
+    [total_q, 16, 576]; returns out [total_q, 16, 512].  kv_indptr has batch + 1 entries."""
+    for name, t in (("q", q), ("kv_packed", kv_packed), ("kv_scale", kv_scale), ("kv_indptr", kv_indptr),
+                    ("qo_indptr", qo_indptr), ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len)):
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor on q's device")
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[1] != NUM_HEADS or q.shape[2] != QK_DIM:
+        raise ValueError("q must be bf16 [total_q, 16, 576]")
+    for name, t in (("kv_indptr", kv_indptr), ("qo_indptr", qo_indptr), ("kv_indices", kv_indices),
+                    ("kv_last_page_len", kv_last_page_len)):
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    batch, total_q = kv_indptr.numel() - 1, q.shape[0]
+    if out is None:
+        out = torch.empty(total_q, NUM_HEADS, V_DIM, dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(max(batch, total_q, 1), q.device)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    with torch.cuda.device(q.device):
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = _lib.mla_decode_mxfp4_paged_ws(q.data_ptr(), kv_packed.data_ptr(), kv_scale.data_ptr(), ptr(qo_indptr),
+                                            kv_indptr.data_ptr(), ptr(kv_indices), ptr(kv_last_page_len), page_size,
+                                            num_pages, out.data_ptr(), batch, total_q, float(sm_scale), s.cuda_stream,
+                                            workspace.data_ptr(), workspace.numel())
+    if rc != _lib.MLA_OK:
+        raise _lib.MlaError(rc, "mla_decode_mxfp4_paged_ws")
+    return out
+
+
+def decode_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, kv_scale: torch.Tensor, kv_indptr: torch.Tensor,
+               sm_scale: float, qo_indptr: torch.Tensor | None = None, out: torch.Tensor | None = None,
+               stream: torch.cuda.Stream | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode against fp8 (e4m3) KV with one per-tensor scale (see mla_decode_fp8_ws).
+    kv_fp8: uint8 (or float8_e4m3fn) [rows, 576]; kv_scale: float32 CUDA tensor holding the
+    scale; q [total_q, 16, 576] bf16; returns out [total_q, 16, 512] bf16."""
+    if kv_fp8.dtype == torch.float8_e4m3fn:
+        kv_fp8 = kv_fp8.view(torch.uint8)
+    for name, t in (("q", q), ("kv_fp8", kv_fp8), ("kv_scale", kv_scale), ("kv_indptr", kv_indptr),
+                    ("qo_indptr", qo_indptr)):
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor on q's device")
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[1] != NUM_HEADS or q.shape[2] != QK_DIM:
+        raise ValueError("q must be bf16 [total_q, 16, 576]")
+    if kv_fp8.dtype != torch.uint8 or kv_fp8.shape[-1] != QK_DIM:
+        raise ValueError("kv_fp8 must be uint8 [rows, 576] (e4m3 bytes)")
+    if kv_scale.dtype != torch.float32 or kv_scale.numel() < 1:
+        raise ValueError("kv_scale must be a float32 tensor holding the per-tensor scale")
+    batch, total_q = kv_indptr.numel() - 1, q.shape[0]
+    if out is None:
+        out = torch.empty(total_q, NUM_HEADS, V_DIM, dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(max(batch, total_q, 1), q.device)
+    with torch.cuda.device(q.device):
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = _lib.mla_decode_fp8_ws(q.data_ptr(), kv_fp8.data_ptr(), kv_scale.data_ptr(),
+                                    qo_indptr.data_ptr() if qo_indptr is not None else None, kv_indptr.data_ptr(),
+                                    kv_fp8.numel() // QK_DIM, out.data_ptr(), batch, total_q, float(sm_scale),
+                                    s.cuda_stream, workspace.data_ptr(), workspace.numel())
+    if rc != _lib.MLA_OK:
+        raise _lib.MlaError(rc, "mla_decode_fp8_ws")
+    return out
+
+
 def device_status(stream: torch.cuda.Stream | None = None, workspace: torch.Tensor | None = None) -> int:
     """Synchronise and read the device status bits of the last call (see mla_device_status)."""
     s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream

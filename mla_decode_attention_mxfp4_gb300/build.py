@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libmla_mxfp4.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = ["mla_api.cu"]
-DEPS = ["mla_api.cu", "mla_kernels.cuh", "ptx.cuh"]
+DEPS = ["mla_api.cu", "mla_kernels.cuh", "mla_fp8_kernel.cuh", "ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

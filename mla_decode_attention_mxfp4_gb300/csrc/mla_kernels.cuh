@@ -95,27 +95,53 @@ constexpr int kDeviceBadIndptr = 1;
 constexpr int kDeviceTimeout = 2;
 
 // meta[] fields written by the partition kernel
-enum MetaField { kMetaN = 0, kMetaPer = 1, kMetaGeff = 2, kMetaStatus = 3 };
+enum MetaField { kMetaN = 0, kMetaPer = 1, kMetaGeff = 2, kMetaStatus = 3, kMetaRows = 4 };
 
 // Partial slots: range g's first segment writes slot 2g and its last segment slot 2g + 1
 // when they are parts of split sequences (any other segment of a range is a whole
 // sequence).  A sequence b split over ranges f..l therefore has its partials in slots
 // 2f + (b starts after range f's first row), 2(f+1), ..., 2l.
 
+// "Sequences" below are query rows: with one query row per sequence they are the sequences
+// themselves; with several (qo_indptr) each query row is its own problem over its
+// sequence's KV rows.  ipc is the prefix of their KV lengths in the logical token stream the
+// CTAs split; phys maps a query row's logical rows to physical KV rows.
 struct Workspace {
   int* meta;          // [16]
-  int* ipc;           // [B+1] sanitised indptr
+  int* ipc;           // [S+1] logical token offsets (the sanitised kv_indptr in the plain layout)
   int4* cta_desc;     // [G][2]: range g = {r0, r1, first sequence b, ipc[b]}, {ipc[b+1], -, -, -}
   float* part_lse;    // [2G][16]   log2-sum-exp of each partial
   float* part_acc;    // [2G][16][512] normalised partial output
-  uint8_t* qhat;      // [B][kQhatBytes] query operand of each sequence, in its shared-memory image
-  float* qch;         // [B][16] score factor of each head: sm_scale * log2(e) * 2^E_h
+  uint8_t* qhat;      // [S][kQhatBytes] query operand of each sequence, in its shared-memory image
+  float* qch;         // [S][16] score factor of each head: sm_scale * log2(e) * 2^E_h
+  int* kvc;           // [Bkv+1] sanitised kv_indptr (general layout only)
+  int* qoc;           // [Bkv+1] sanitised qo_indptr for more than kPartSmemSeqs sequences (general layout)
+  int* phys;          // [S] first physical row, or first entry of kv_indices (general layout only)
 };
+
+// Layout of the KV rows beyond the plain one (kv_indptr rows, one query row per sequence).
+struct RowMap {
+  const int32_t* qo_indptr;   // [Bkv+1] query rows of each sequence, or null (row b = sequence b)
+  const int32_t* kv_indices;  // paged: page ids, kv_indptr counting entries of it; null: kv_indptr counts rows
+  const int32_t* last_len;    // paged: rows used in each sequence's last page, [Bkv]
+  int Bkv;                    // sequences (kv_indptr holds Bkv + 1 entries)
+  int page_size;              // paged: rows per page
+  int num_pages;              // paged: pages the KV buffers hold
+  int kv_rows;                // > 0: rows the KV buffer holds (kv_indptr is clamped to it, and flagged)
+};
+constexpr int kRowModePlain = 0, kRowModeContig = 1, kRowModePaged = 2;
+// Longer sequences are clamped (and flagged); 1024 of them still sum within int32 in the
+// partition kernel's block scan.
+constexpr int kMaxRowsPerQuery = 1 << 20;
 
 // ---- shared-memory and tensor-memory map of mla_split_kernel ---------------
 constexpr int kStagePackedBytes = kTile * kPacked;                   // 36864
 constexpr int kStageScaleBytes = 2432;                               // >= 128*18 + 32, mult of 16
 constexpr int kStageBytes = kStagePackedBytes + kStageScaleBytes;    // 39296
+// The last word of a stage's scale area holds the offset (0..15) at which the tile's first
+// scale byte landed (written by the producer before the stage's copies are announced).
+constexpr int kStageMisOff = kStagePackedBytes + kStageScaleBytes - 4;
+static_assert(kStageScaleBytes - 4 >= 16 + ((kTile * kNScale + 15) / 16) * 16, "misalignment slot");
 constexpr int kQhatBytes = 32 * kDqk;                                // 18432: e4m3 hi + lo query parts
 
 // Tensor memory (32-bit columns, lane = token of the tile / row of M):
@@ -178,6 +204,9 @@ struct SplitParams {
   const uint8_t* kv;
   const uint8_t* sc;  // the 16-byte boundary at or below kv_scale (kv_scale = sc + sc_mis)
   int sc_mis;         // kv_scale's offset from that boundary (0..15)
+  int rmode;          // kRowMode*: how logical token rows map to physical KV rows
+  const int32_t* kv_indices;  // paged: page ids
+  int page_size, num_pages;   // paged
   __nv_bfloat16* out;
   Workspace ws;
   int B;
@@ -338,12 +367,15 @@ __device__ __forceinline__ void build_qhat_head(const __nv_bfloat16* __restrict_
 // kv_null: the KV buffers are absent (NULL), so no row may be read.
 // Blocks 1..: the query operand of sequences 2(x-1) and 2(x-1)+1 (warp w: head w % 16),
 // so the split kernel copies it instead of building it at every segment start.
+// B is the number of query rows (sequences of the logical stream).  With rm.qo_indptr or
+// rm.kv_indices set (the general layout), block 0 first derives every query row's KV length
+// and physical start from the sequence it belongs to.
 constexpr int kPartThreads = 1024;
 constexpr int kQhatSeqsPerBlock = kPartThreads / 32 / kHeads;  // 2
-__global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
+__global__ void __launch_bounds__(kPartThreads, 1) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
                                                                      int G, int kv_null, Workspace ws,
                                                                      const __nv_bfloat16* __restrict__ q,
-                                                                     float sm_scale) {
+                                                                     float sm_scale, RowMap rm) {
   grid_launch_dependents();  // the split kernel's prologue may run alongside
   // Launched with programmatic serialization, this grid may be resident before the
   // preceding kernel in the stream (the previous call's merge kernel, or whatever wrote
@@ -359,25 +391,132 @@ __global__ void __launch_bounds__(kPartThreads) mla_partition_kernel(const int32
   __shared__ int s_bad;
   __shared__ int s_ipc[kPartSmemSeqs + 1];  // copy of ipc for batch <= kPartSmemSeqs
   const bool in_smem = B <= kPartSmemSeqs;
+  const bool general = rm.qo_indptr != nullptr || rm.kv_indices != nullptr;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  const int hi = kv_null ? 0 : max(indptr[B], 0);
-  // ipc[i] = clamp(max(indptr[0..i]), 0, indptr[B]); every row index stays below indptr[B]
-  int carry = INT_MIN;
-  for (int base = 0; base <= B; base += 1024) {
-    const int i = base + tid;
-    int v = (i <= B) ? indptr[i] : INT_MIN;
-    if (i <= B && (v < 0 || v > hi || (i > 0 && v < indptr[i - 1]))) s_bad = 1;
-    int tot;
-    int pm = block_inclusive_scan<true>(v, warp_tot, tot);
-    pm = max(pm, carry);
-    if (i <= B) {
-      const int c = min(max(pm, 0), hi);
-      ws.ipc[i] = c;
-      if (in_smem) s_ipc[i] = c;
+  if (!general) {
+    int hi = kv_null ? 0 : max(indptr[B], 0);
+    if (rm.kv_rows > 0 && hi > rm.kv_rows) {
+      hi = rm.kv_rows;
+      if (tid == 0) s_bad = 1;
     }
-    carry = max(carry, tot);
+    // ipc[i] = clamp(max(indptr[0..i]), 0, indptr[B]); every row index stays below indptr[B]
+    int carry = INT_MIN;
+    for (int base = 0; base <= B; base += 1024) {
+      const int i = base + tid;
+      int v = (i <= B) ? indptr[i] : INT_MIN;
+      if (i <= B && (v < 0 || v > hi || (i > 0 && v < indptr[i - 1]))) s_bad = 1;
+      int tot;
+      int pm = block_inclusive_scan<true>(v, warp_tot, tot);
+      pm = max(pm, carry);
+      if (i <= B) {
+        const int c = min(max(pm, 0), hi);
+        ws.ipc[i] = c;
+        if (in_smem) s_ipc[i] = c;
+      }
+      carry = max(carry, tot);
+      __syncthreads();
+    }
+    if (tid == 0) ws.meta[kMetaRows] = hi;
+  } else {
+    // 1. kv_indptr over the Bkv sequences -> kvc, sanitised as above (counting rows, or
+    //    entries of kv_indices when paged)
+    const int Bkv = rm.Bkv;
+    const bool paged = rm.kv_indices != nullptr;
+    int hi = kv_null ? 0 : max(indptr[Bkv], 0);
+    if (!paged && rm.kv_rows > 0 && hi > rm.kv_rows) {
+      hi = rm.kv_rows;
+      if (tid == 0) s_bad = 1;
+    }
+    int carry = INT_MIN;
+    for (int base = 0; base <= Bkv; base += 1024) {
+      const int i = base + tid;
+      int v = (i <= Bkv) ? indptr[i] : INT_MIN;
+      if (i <= Bkv && (v < 0 || v > hi || (i > 0 && v < indptr[i - 1]))) s_bad = 1;
+      int tot;
+      int pm = block_inclusive_scan<true>(v, warp_tot, tot);
+      pm = max(pm, carry);
+      if (i <= Bkv) ws.kvc[i] = min(max(pm, 0), hi);
+      carry = max(carry, tot);
+      __syncthreads();
+    }
+    // 2. qo_indptr -> its sanitised copy (shared memory for up to kPartSmemSeqs sequences;
+    //    s_ipc is free until step 3 has read it), clamped to [0, B]
+    int* qoc = nullptr;
+    if (rm.qo_indptr) {
+      qoc = Bkv <= kPartSmemSeqs && !in_smem ? s_ipc : ws.qoc;
+      carry = INT_MIN;
+      for (int base = 0; base <= Bkv; base += 1024) {
+        const int i = base + tid;
+        int v = (i <= Bkv) ? rm.qo_indptr[i] : INT_MIN;
+        if (i <= Bkv && (v < 0 || v > B || (i > 0 && v < rm.qo_indptr[i - 1]))) s_bad = 1;
+        int tot;
+        int pm = block_inclusive_scan<true>(v, warp_tot, tot);
+        pm = max(pm, carry);
+        if (i <= Bkv) qoc[i] = min(max(pm, 0), B);
+        carry = max(carry, tot);
+        __syncthreads();
+      }
+      if (tid == 0 && (rm.qo_indptr[0] != 0 || rm.qo_indptr[Bkv] != B)) s_bad = 1;
+    }
+    __threadfence_block();
     __syncthreads();
+    // 3. every query row j: its sequence, KV length and physical start; ipc = exclusive prefix
+    //    of the lengths (rows past the total that int32 offsets can hold get length 0)
+    long long lcarry = 0;
+    for (int base = 0; base < B + 1024; base += 1024) {
+      if (base > B) break;
+      const int j = base + tid;
+      int len = 0, ph = 0, b = -1;
+      if (j < B) {
+        if (qoc) {  // the last sequence whose first query row is <= j, if j lies inside it
+          int lo = 0, hi2 = Bkv - 1;
+          while (lo < hi2) {
+            const int mid = (lo + hi2 + 1) >> 1;
+            if (qoc[mid] <= j) lo = mid;
+            else hi2 = mid - 1;
+          }
+          b = (Bkv > 0 && qoc[lo] <= j && j < qoc[lo + 1]) ? lo : -1;
+        } else {
+          b = j < Bkv ? j : -1;
+        }
+        if (b >= 0) {
+          const int k0 = ws.kvc[b], k1 = ws.kvc[b + 1];
+          if (paged) {
+            const int np = k1 - k0;
+            int last = 0;
+            if (np > 0) {
+              last = rm.last_len[b];
+              if (last < 1 || last > rm.page_size) {
+                s_bad = 1;
+                last = min(max(last, 1), rm.page_size);
+              }
+            }
+            const long long L = np > 0 ? (long long)(np - 1) * rm.page_size + last : 0;
+            len = (int)min(L, (long long)kMaxRowsPerQuery);
+            if (L > kMaxRowsPerQuery) s_bad = 1;
+          } else {
+            len = min(k1 - k0, kMaxRowsPerQuery);
+            if (k1 - k0 > kMaxRowsPerQuery) s_bad = 1;
+          }
+          ph = k0;
+        }
+      }
+      __syncthreads();  // every row's qoc lookups are done before s_ipc (possibly holding qoc) is rewritten
+      int tot;
+      const int incl = block_inclusive_scan<false>(len, warp_tot, tot);
+      const long long start = lcarry + incl - len;
+      if (j <= B) {
+        const int c = (int)min(start, (long long)INT_MAX);
+        ws.ipc[j] = c;
+        if (in_smem) s_ipc[j] = c;
+        if (start > INT_MAX) s_bad = 1;
+      }
+      if (j < B) ws.phys[j] = ph;
+      lcarry += tot;
+      __syncthreads();
+    }
+    if (tid == 0) ws.meta[kMetaRows] = paged ? (int)min((long long)rm.num_pages * rm.page_size, (long long)INT_MAX) : hi;
   }
   __threadfence_block();
   __syncthreads();
@@ -484,11 +623,13 @@ __device__ __forceinline__ int next_reference(int T, int r_prev, int r_max, bool
 // group, which also orders every part's V^T copy of the previous tile, read from the K
 // buffer about to be overwritten, before any part overwrites it.  Part 0 stores R in
 // tensor-memory column r_col for the softmax group.  Returns R.
-__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int t0, int n, int t, int part, int q4,
-                                              uint32_t a_lane, uint32_t r_col, int* tq, int sc_mis, int r_prev,
-                                              int r_max, bool seg_first) {
+__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, int part, int q4, uint32_t a_lane,
+                                              uint32_t r_col, int* tq, int r_prev, int r_max, bool seg_first) {
   const bool valid = t < n;
-  const uint8_t* sb = st + kStagePackedBytes + (int)((sc_mis + (long long)t0 * kNScale) & 15) + t * kNScale;
+  // where the tile's first scale byte landed (0..15): the producer's note in the stage, masked
+  // so that a stage that never landed (a wait that gave up) is still read in bounds
+  const int mis = *reinterpret_cast<const int*>(st + kStageMisOff) & 15;
+  const uint8_t* sb = st + kStagePackedBytes + mis + t * kNScale;
   constexpr int kNb = kNScale / kDqParts;  // consecutive blocks b0 .. b0 + kNb - 1 of this part
   static_assert(kNScale % kDqParts == 0 && kNb % 2 == 0, "pairs of blocks per part");
   const int b0 = part * kNb;
@@ -619,11 +760,25 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    // scale byte x of token row r is at sc[sc_mis + 18r]; the bytes in use end at scale_end, and
+    // scale byte x of physical row r is at sc[sc_mis + 18r]; the bytes in use end at scale_end, and
     // the buffer's first 16-byte boundary is head16
-    const long long scale_end = p.sc_mis + (long long)p.ws.ipc[p.B] * kNScale;
+    const long long scale_end = p.sc_mis + (long long)p.ws.meta[kMetaRows] * kNScale;
     const long long scale_end16 = scale_end & ~15LL;
     const long long head16 = (p.sc_mis + 15) & ~15LL;
+    // Paged layout: the run of the tile's tokens that starts at tile row i lies in one page:
+    // `cnt` rows from physical row `row`.
+    auto chunk_at = [&](const TileIter& ti, int i, long long& row, int& cnt) {
+      {
+        const int pos = ti.t0 - p.ws.ipc[ti.b] + i, pg = pos / p.page_size, off = pos - pg * p.page_size;
+        int page = p.kv_indices[p.ws.phys[ti.b] + pg];
+        if (page < 0 || page >= p.num_pages) {  // clamped into the buffers, and flagged
+          atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
+          page = min(max(page, 0), max(p.num_pages - 1, 0));
+        }
+        row = (long long)page * p.page_size + off;
+        cnt = min(p.page_size - off, ti.n - i);
+      }
+    };
     int k = 0;
     if (!p.stall_producer) do {
       const int s = k % kStages;
@@ -633,22 +788,71 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       if (it.first && j >= 2 && !wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted))
         break;
       uint8_t* st = smem + kOffStages + s * kStageBytes;
-      // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
-      // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
-      // buffer's first boundary and past its last one by plain loads
-      const long long b0 = p.sc_mis + (long long)it.t0 * kNScale, b1 = p.sc_mis + (long long)(it.t0 + it.n) * kNScale;
-      const long long a0 = b0 & ~15LL;
-      const long long c0 = a0 > head16 ? a0 : head16;
-      long long a1 = (b1 + 15) & ~15LL;
-      if (a1 > scale_end16) a1 = scale_end16;
       uint8_t* sdst = st + kStagePackedBytes;
-      for (long long x = b0; x < b1 && x < c0; ++x) sdst[x - a0] = p.sc[x];
-      for (long long x = (a1 > c0 ? a1 : c0); x < b1; ++x) sdst[x - a0] = p.sc[x];
-      uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > c0 ? (uint32_t)(a1 - c0) : 0u);
-      if (it.first) bytes += kQhatBytes;
-      mbar_arrive_expect_tx(&bar_full[s], bytes);
-      bulk_g2s(st, p.kv + (long long)it.t0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
-      if (a1 > c0) bulk_g2s(sdst + (c0 - a0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+      if (p.rmode != kRowModePaged) {
+        // one run of rows from physical row row0 (row0 = t0 in the plain layout)
+        const long long row0 =
+            it.t0 + (p.rmode == kRowModeContig ? (long long)p.ws.phys[it.b] - p.ws.ipc[it.b] : 0LL);
+        // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
+        // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
+        // buffer's first boundary and past its last one by plain loads
+        const long long b0 = p.sc_mis + row0 * kNScale, b1 = b0 + (long long)it.n * kNScale;
+        const long long a0 = b0 & ~15LL;
+        const long long c0 = a0 > head16 ? a0 : head16;
+        long long a1 = (b1 + 15) & ~15LL;
+        if (a1 > scale_end16) a1 = scale_end16;
+        for (long long x = b0; x < b1 && x < c0; ++x) sdst[x - a0] = p.sc[x];
+        for (long long x = (a1 > c0 ? a1 : c0); x < b1; ++x) sdst[x - a0] = p.sc[x];
+        *reinterpret_cast<int*>(st + kStageMisOff) = (int)(b0 & 15);
+        uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > c0 ? (uint32_t)(a1 - c0) : 0u);
+        if (it.first) bytes += kQhatBytes;
+        mbar_arrive_expect_tx(&bar_full[s], bytes);
+        bulk_g2s(st, p.kv + row0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
+        if (a1 > c0) bulk_g2s(sdst + (c0 - a0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+      } else {
+        // Paged: one run per page the tile touches.  A run's scale bytes [g0, g1) land at stage
+        // offset dst0 + (x - g0), dst0 = M + 18 i: the 16-byte chunks [c0, a1) by bulk copy when
+        // source and destination agree modulo 16, the other bytes by plain loads.  At the tile's
+        // own ends the bulk range may round outwards (the extra bytes land outside the tile's
+        // part of the area); between runs it rounds inwards.  Pass 1 does the plain loads and
+        // counts the bulk bytes; the stage is then announced with its byte count; pass 2
+        // issues the bulk copies.
+        long long row0;
+        int cnt0;
+        chunk_at(it, 0, row0, cnt0);
+        const int M = (int)((p.sc_mis + row0 * kNScale) & 15);
+        uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int i = 0; i < it.n;) {
+            long long row;
+            int cnt;
+            chunk_at(it, i, row, cnt);
+            const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
+            const long long dst0 = M + (long long)i * kNScale;
+            long long c0 = g1, a1 = g1;  // no bulk range
+            if (((g0 - dst0) & 15) == 0) {
+              c0 = i == 0 ? (g0 & ~15LL) : ((g0 + 15) & ~15LL);
+              a1 = i + cnt == it.n ? ((g1 + 15) & ~15LL) : (g1 & ~15LL);
+              if (c0 < head16) c0 = head16;
+              if (a1 > scale_end16) a1 = scale_end16;
+              if (a1 < c0) a1 = c0;
+            }
+            if (pass == 0) {
+              for (long long x = g0; x < g1 && x < c0; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+              for (long long x = (a1 > g0 ? a1 : g0); x < g1; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+              bytes += (uint32_t)cnt * kPacked + (uint32_t)(a1 - c0);
+            } else {
+              bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
+              if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+            }
+            i += cnt;
+          }
+          if (pass == 0) {
+            *reinterpret_cast<int*>(st + kStageMisOff) = M;
+            mbar_arrive_expect_tx(&bar_full[s], bytes);
+          }
+        }
+      }
       if (it.first)
         bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
                  &bar_full[s], pol_q);
@@ -756,8 +960,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     wait_or_flag(&bar_full[0], 0, p, aborted);
     int* tq = reinterpret_cast<int*>(smem + kOffStq);  // [2 tile parities][12 dequant warps]
     // reference exponent of the last converted tile and the largest of its segment
-    int r_ref = k_tile_to_tmem(smem + kOffStages, it.t0, it.n, t, part, q4, t_lane + kColA, t_lane + kColSt, tq,
-                               p.sc_mis, 0, 0, true);
+    int r_ref = k_tile_to_tmem(smem + kOffStages, it.n, t, part, q4, t_lane + kColA, t_lane + kColSt, tq, 0, 0,
+                               true);
     int r_max = r_ref;
     tc_wait_st();
     tc_fence_before();
@@ -783,9 +987,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         tc_fence_after();
         // the reference of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3,
         // which finished before P.V of tile k-3 (waited for two iterations ago)
-        r_ref = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.t0, it.n, t, part, q4,
+        r_ref = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.n, t, part, q4,
                                t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
-                               tq + ((k + 1) & 1) * kDqWarps, p.sc_mis, r_ref, r_max, it.first);
+                               tq + ((k + 1) & 1) * kDqWarps, r_ref, r_max, it.first);
         r_max = it.first ? r_ref : max(r_max, r_ref);
         tc_wait_st();
         tc_fence_before();

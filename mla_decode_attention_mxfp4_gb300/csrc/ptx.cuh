@@ -285,3 +285,34 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
 }
 
 }  // namespace mla
+
+namespace mla {
+// ---- TMA tensor copies and 128-byte-swizzled operands ---------------------------------
+// 2D tile of a tensor map -> shared memory, completing on an mbarrier (bytes of the whole box,
+// out-of-range elements filled with zero).  x (the inner coordinate) must be a multiple of 16
+// bytes; dst 1024-byte aligned for a 128-byte swizzle.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+// Shared-memory matrix descriptor with the 128-byte swizzle (rows of 128 bytes, 8-row atoms of
+// 1024 bytes, 16-byte chunks XOR-permuted by the row within the atom).  K-major: sbo = stride
+// between 8-row groups along M/N, lbo unused; MN-major: sbo = stride between 8-row groups along
+// K, lbo = stride between 128-byte column blocks along M/N.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for this architecture
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+}  // namespace mla

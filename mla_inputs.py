@@ -173,3 +173,121 @@ def make_custom(lens, seed: int = 1234, q_std: float = 1.0) -> DecodeInputs:
         torch.empty(0, PACKED_BYTES, dtype=torch.uint8), torch.empty(0, NUM_SCALES, dtype=torch.uint8))
     return DecodeInputs(q=q, kv_packed=packed, kv_scale=scale,
                         kv_indptr=indptr.to(torch.int32), sm_scale=SM_SCALE)
+
+
+def scatter_into_pages(d: DecodeInputs, page_size: int, seed: int, spare_pages: int = 3,
+                       fill_packed: int = 0x77, fill_scale: int = 200):
+    """Place every sequence's KV rows, in order, into randomly chosen pages of a larger buffer
+    (the paged layout: page p holds rows [p*page_size, (p+1)*page_size)).  Unused rows hold
+    junk.  Returns (kv_packed, kv_scale, kv_indptr over pages, kv_indices, kv_last_page_len,
+    num_pages); a sequence without rows has no page (its last-page length is 1, unused)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = (d.kv_indptr[1:] - d.kv_indptr[:-1]).tolist()
+    npages = [(n + page_size - 1) // page_size for n in lens]
+    total = sum(npages) + spare_pages
+    perm = torch.randperm(total, generator=g).tolist()
+    kp = torch.full((total * page_size, PACKED_BYTES), fill_packed, dtype=torch.uint8)
+    ks = torch.full((total * page_size, NUM_SCALES), fill_scale, dtype=torch.uint8)
+    indptr, indices, last = [0], [], []
+    nxt = 0
+    for b, n in enumerate(lens):
+        r0 = int(d.kv_indptr[b])
+        for j in range(npages[b]):
+            page = perm[nxt]
+            nxt += 1
+            indices.append(page)
+            rows = min(page_size, n - j * page_size)
+            kp[page * page_size: page * page_size + rows] = d.kv_packed[r0 + j * page_size: r0 + j * page_size + rows]
+            ks[page * page_size: page * page_size + rows] = d.kv_scale[r0 + j * page_size: r0 + j * page_size + rows]
+        indptr.append(len(indices))
+        last.append(n - (npages[b] - 1) * page_size if npages[b] else 1)
+    return (kp, ks, torch.tensor(indptr, dtype=torch.int32), torch.tensor(indices, dtype=torch.int32),
+            torch.tensor(last, dtype=torch.int32), total)
+
+
+def query_rows(q_per_seq, seed: int, q_std: float = 1.0):
+    """Several query rows per sequence: bf16 q [total_q,16,576] and qo_indptr [B+1]."""
+    g = torch.Generator().manual_seed(seed)
+    qo = torch.zeros(len(q_per_seq) + 1, dtype=torch.int32)
+    if len(q_per_seq):
+        qo[1:] = torch.cumsum(torch.as_tensor(list(q_per_seq), dtype=torch.int64), 0).to(torch.int32)
+    q = (torch.randn(int(qo[-1]), NUM_HEADS, QK_DIM, generator=g) * q_std).to(torch.bfloat16)
+    return q, qo
+
+
+@dataclass
+class Fp8Inputs:
+    q: torch.Tensor          # bf16 [total_q,16,576]
+    kv_fp8: torch.Tensor     # uint8 [rows,576]: e4m3 ("fn") bytes
+    kv_scale: float          # the per-tensor scale: K = e4m3(kv_fp8) * kv_scale
+    kv_indptr: torch.Tensor  # int32 [B+1]
+    sm_scale: float
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_indptr.numel()) - 1
+
+    @property
+    def total_kv(self) -> int:
+        return int(self.kv_fp8.shape[0])
+
+    def algorithmic_bytes(self) -> int:
+        """Q + fp8 KV + bf16 output bytes of one decode call."""
+        return self.q.numel() * 2 + self.kv_fp8.numel() + self.q.shape[0] * NUM_HEADS * V_DIM * 2
+
+
+def quantize_fp8(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """e4m3 bytes of x / scale (round to nearest even; |x| / scale <= 448 by the choice of scale)."""
+    return (x.to(torch.float32) / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def make_fp8_inputs(w: Workload | str, batch: int | None = None) -> Fp8Inputs:
+    """A workload's shapes and draws (lengths -> Q -> latent KV, as make_inputs) with the KV
+    cache stored as fp8 e4m3 under one per-tensor scale amax / 448 (the largest e4m3 value)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    g = torch.Generator().manual_seed(w.seed)
+    B = w.batch
+    if w.kv_len is None:
+        lens = torch.randint(1, w.ragged_max + 1, (B,), generator=g)
+    else:
+        lens = torch.full((B,), w.kv_len, dtype=torch.int64)
+    q = (torch.randn(B, NUM_HEADS, QK_DIM, generator=g) * w.q_std).to(torch.bfloat16)
+    if w.outlier_frac > 0:
+        k = int(round(w.outlier_frac * QK_DIM))
+        outliers = sorted(torch.randperm(QK_DIM, generator=g)[:k].tolist())
+    else:
+        outliers = []
+    if batch is not None and batch < B:
+        lens, q = lens[:batch], q[:batch].contiguous()
+        B = batch
+    indptr = torch.zeros(B + 1, dtype=torch.int64)
+    indptr[1:] = torch.cumsum(lens, 0)
+    total = int(indptr[-1])
+    lat = torch.empty(total, QK_DIM, dtype=torch.float32)
+    for s0 in range(0, total, CHUNK_TOKENS):
+        e = min(total, s0 + CHUNK_TOKENS)
+        lat[s0:e] = torch.randn(e - s0, QK_DIM, generator=g)
+    if outliers:
+        lat[:, outliers] *= w.outlier_gain
+    amax = float(lat.abs().max()) if total else 1.0
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return Fp8Inputs(q=q, kv_fp8=quantize_fp8(lat, scale), kv_scale=scale,
+                     kv_indptr=indptr.to(torch.int32), sm_scale=SM_SCALE)
+
+
+def make_fp8_custom(lens, seed: int = 1234, q_std: float = 1.0) -> Fp8Inputs:
+    """fp8 inputs with explicit per-sequence lengths."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.as_tensor(list(lens), dtype=torch.int64)
+    B = lens.numel()
+    q = (torch.randn(B, NUM_HEADS, QK_DIM, generator=g) * q_std).to(torch.bfloat16)
+    indptr = torch.zeros(B + 1, dtype=torch.int64)
+    if B:
+        indptr[1:] = torch.cumsum(lens, 0)
+    total = int(indptr[-1])
+    lat = torch.randn(total, QK_DIM, generator=g)
+    amax = float(lat.abs().max()) if total else 1.0
+    scale = amax / 448.0 if amax > 0 else 1.0
+    return Fp8Inputs(q=q, kv_fp8=quantize_fp8(lat, scale) if total else torch.empty(0, QK_DIM, dtype=torch.uint8),
+                     kv_scale=scale, kv_indptr=indptr.to(torch.int32), sm_scale=SM_SCALE)

@@ -68,3 +68,19 @@ def test_product_path_has_no_cpu_fallback():
     with pytest.raises(ValueError):
         api.decode(q, torch.zeros(1, 288, dtype=torch.uint8), torch.zeros(1, 18, dtype=torch.uint8),
                    torch.tensor([0, 1], dtype=torch.int32), 1 / 24)
+
+
+def test_host_argument_checks_of_the_general_entry(L):
+    from mla_decode_attention_mxfp4_gb300 import _lib
+    f = _lib.mla_decode_mxfp4_paged_ws
+    a = dict(q=0x1000, kv=0x2000, sc=0x3000, ip=0x4000, out=0x5000, ws=0x10000)
+    # total_q != batch without query offsets
+    assert f(a["q"], a["kv"], a["sc"], None, a["ip"], None, None, 0, 0, a["out"], 2, 3, 1.0, None, a["ws"],
+             1 << 24) == _lib.MLA_ERR_BAD_LAYOUT
+    # paged without a positive page size or without last-page lengths
+    assert f(a["q"], a["kv"], a["sc"], None, a["ip"], 0x6000, 0x7000, 0, 4, a["out"], 2, 2, 1.0, None, a["ws"],
+             1 << 24) == _lib.MLA_ERR_BAD_LAYOUT
+    assert f(a["q"], a["kv"], a["sc"], None, a["ip"], 0x6000, None, 16, 4, a["out"], 2, 2, 1.0, None, a["ws"],
+             1 << 24) == _lib.MLA_ERR_BAD_LAYOUT
+    assert f(a["q"], a["kv"], a["sc"], None, a["ip"], None, None, 0, 0, a["out"], -1, -1, 1.0, None, a["ws"],
+             1 << 24) == _lib.MLA_ERR_BAD_BATCH
