@@ -30,6 +30,7 @@ constexpr int kVBoxes = kDv / kBoxBytes;              // 4: the V part
 constexpr int kBoxTileBytes = kTile * kBoxBytes;      // 16384
 constexpr int kStageBytes = kBoxes * kBoxTileBytes;   // 81920
 constexpr int kStages = 2;
+constexpr int kPrefetch = 2;  // lookahead of the L2 prefetch in tiles (see the producer)
 constexpr int kSmWarps = 4;
 constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kMmaWarp = 0, kProdWarp = 1, kSmWarp0 = 2;
@@ -134,6 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
+    // Two stages of 80 KB hold too few bytes in flight to cover the load latency, so when tile k
+    // is copied, tile k + kPrefetch (which must wait for a stage) is prefetched into L2: its
+    // copy, once a stage is free, then reads L2.
+    TileIter pf = it;
+    bool pf_ok = true;
+    for (int u = 0; u < kPrefetch && pf_ok; ++u) pf_ok = pf.next();
     int k = 0;
     do {
       const int s = k % kStages;
@@ -148,6 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
       if (it.first)
         bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
                  &bar_full[s], pol_q);
+      if (pf_ok) {  // pf: tile k + kPrefetch
+        const int r = pf.t0 + (p.rmode == kRowModeContig ? p.ws.phys[pf.b] - p.ws.ipc[pf.b] : 0);
+#pragma unroll
+        for (int x = 0; x < kBoxes; ++x) tma_prefetch_2d(&tmap, x * kBoxBytes, r);
+        pf_ok = pf.next();
+      }
       ++k;
     } while (!*abort_word_fp8() && it.next());
     for (int s = 0; s < kStages && s < k; ++s) {  // drain: no copy may still be writing at exit

@@ -767,18 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     const long long head16 = (p.sc_mis + 15) & ~15LL;
     // Paged layout: the run of the tile's tokens that starts at tile row i lies in one page:
     // `cnt` rows from physical row `row`.
-    auto chunk_at = [&](const TileIter& ti, int i, long long& row, int& cnt) {
-      {
-        const int pos = ti.t0 - p.ws.ipc[ti.b] + i, pg = pos / p.page_size, off = pos - pg * p.page_size;
-        int page = p.kv_indices[p.ws.phys[ti.b] + pg];
-        if (page < 0 || page >= p.num_pages) {  // clamped into the buffers, and flagged
-          atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
-          page = min(max(page, 0), max(p.num_pages - 1, 0));
-        }
-        row = (long long)page * p.page_size + off;
-        cnt = min(p.page_size - off, ti.n - i);
-      }
-    };
+    // Paged layout: the sequence's logical start and its first kv_indices entry are loaded
+    // once per segment; a tile's page ids (it touches at most kTilePages pages when
+    // page_size >= 16) are loaded together into registers, then both passes walk the runs.
+    constexpr int kTilePages = kTile / 16 + 1;
+    int seg_b = -1, seg_pos0 = 0, seg_ix0 = 0;
     int k = 0;
     if (!p.stall_producer) do {
       const int s = k % kStages;
@@ -817,16 +810,57 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         // part of the area); between runs it rounds inwards.  Pass 1 does the plain loads and
         // counts the bulk bytes; the stage is then announced with its byte count; pass 2
         // issues the bulk copies.
+        if (it.b != seg_b) {
+          seg_b = it.b;
+          seg_pos0 = p.ws.ipc[seg_b];
+          seg_ix0 = p.ws.phys[seg_b];
+        }
+        const int ps = p.page_size;
+        const int pos0 = it.t0 - seg_pos0;
+        const int pg0 = pos0 / ps, off0 = pos0 - pg0 * ps;
+        const int npg = (off0 + it.n + ps - 1) / ps;  // pages the tile touches
+        int pid[kTilePages];
+        const bool in_regs = npg <= kTilePages;
+        if (in_regs) {
+#pragma unroll
+          for (int u = 0; u < kTilePages; ++u) pid[u] = u < npg ? p.kv_indices[seg_ix0 + pg0 + u] : 0;
+#pragma unroll
+          for (int u = 0; u < kTilePages; ++u) {
+            if (u < npg && (pid[u] < 0 || pid[u] >= p.num_pages)) {  // clamped into the buffers, and flagged
+              atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
+              pid[u] = min(max(pid[u], 0), max(p.num_pages - 1, 0));
+            }
+          }
+        }
+        // run u (u < npg): tile rows [i, i + cnt) from physical row `row`
+        auto run = [&](int u, int& i, int& cnt, long long& row) {
+          int page = 0;
+          if (in_regs) {
+#pragma unroll
+            for (int v = 0; v < kTilePages; ++v)
+              if (v == u) page = pid[v];
+          } else {
+            page = p.kv_indices[seg_ix0 + pg0 + u];
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
+              page = min(max(page, 0), max(p.num_pages - 1, 0));
+            }
+          }
+          const int off = u == 0 ? off0 : 0;
+          i = u == 0 ? 0 : ps * u - off0;
+          cnt = min(ps - off, it.n - i);
+          row = (long long)page * ps + off;
+        };
+        int i0, c0n;
         long long row0;
-        int cnt0;
-        chunk_at(it, 0, row0, cnt0);
+        run(0, i0, c0n, row0);
         const int M = (int)((p.sc_mis + row0 * kNScale) & 15);
         uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
         for (int pass = 0; pass < 2; ++pass) {
-          for (int i = 0; i < it.n;) {
+          for (int u = 0; u < npg; ++u) {
+            int i, cnt;
             long long row;
-            int cnt;
-            chunk_at(it, i, row, cnt);
+            run(u, i, cnt, row);
             const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
             const long long dst0 = M + (long long)i * kNScale;
             long long c0 = g1, a1 = g1;  // no bulk range
@@ -845,7 +879,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
               bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
               if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
             }
-            i += cnt;
           }
           if (pass == 0) {
             *reinterpret_cast<int*>(st + kStageMisOff) = M;
