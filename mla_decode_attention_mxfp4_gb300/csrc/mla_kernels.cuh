@@ -191,8 +191,8 @@ constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230
 constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136: tensor-memory address
 constexpr int kOffAbort = kOffTmem + 4;                                   // abort word (bounded waits)
 constexpr int kOffBar = kOffTmem + 16;                                    // 231152
-constexpr int kNumBars = 15;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231272
+constexpr int kNumBars = 17;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231288
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
@@ -618,11 +618,11 @@ __device__ __forceinline__ int next_reference(int T, int r_prev, int r_max, bool
 // further below are zero.  Tokens past the tile are zero.  Token t = this thread's lane of
 // the quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
 // pair's bytes are loaded while this pair is converted; one 16-column store per pair).
-// Every dequant warp first takes the largest scale byte of its blocks over its 32 tokens;
-// the twelve maxima meet in tq (this tile's parity) behind a barrier of the whole dequant
-// group, which also orders every part's V^T copy of the previous tile, read from the K
-// buffer about to be overwritten, before any part overwrites it.  Part 0 stores R in
-// tensor-memory column r_col for the softmax group.  Returns R.
+// Every dequant thread first takes the largest scale byte of its blocks; the group decides
+// R behind a barrier of the whole dequant group, which also orders every part's V^T copy of
+// the previous tile, read from the K buffer about to be overwritten, before any part
+// overwrites it.  Part 0 stores R in tensor-memory column r_col for the softmax group.
+// Returns R.
 __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, int part, int q4, uint32_t a_lane,
                                               uint32_t r_col, int* tq, int r_prev, int r_max, bool seg_first) {
   const bool valid = t < n;
@@ -639,13 +639,20 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, i
 #pragma unroll
     for (int j = 0; j < kNb; ++j) m = max(m, (int)sp[j]);
   }
-  m = (int)__reduce_max_sync(0xffffffffu, (unsigned)m);
-  if ((t & 31) == 0) tq[part * 4 + q4] = m;
-  named_sync(kBarDqTile, kDqThreads);
-  int T = 0;
+  // Within a segment the reference usually stays: T_k in [r_prev - kRefSlack, r_prev] keeps it,
+  // and two reducing barriers (every block at most r_prev; some block at least r_prev -
+  // kRefSlack) decide that without exchanging maxima.  Otherwise the warps' maxima meet in tq.
+  int R = r_prev;
+  if (seg_first || !named_sync_and(kBarDqTile, kDqThreads, m <= r_prev) ||
+      !named_sync_or(kBarDqTile, kDqThreads, m >= r_prev - kRefSlack)) {
+    m = (int)__reduce_max_sync(0xffffffffu, (unsigned)m);
+    if ((t & 31) == 0) tq[part * 4 + q4] = m;
+    named_sync(kBarDqTile, kDqThreads);
+    int T = 0;
 #pragma unroll
-  for (int i = 0; i < kDqWarps; ++i) T = max(T, tq[i]);
-  const int R = next_reference(T, r_prev, r_max, seg_first);
+    for (int i = 0; i < kDqWarps; ++i) T = max(T, tq[i]);
+    R = next_reference(T, r_prev, r_max, seg_first);
+  }
   if (part == 0) {
     const uint32_t rv[1] = {(uint32_t)R};
     tmem_st1(r_col, rv);
@@ -717,9 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bar_qfree = bars + 6;     // [2] Qhat buffer b read by the last QK^T of its segment (MMA commit)
   uint64_t* bar_kready = bars + 8;    // [2] K tile in tensor-memory buffer b ready, its Qhat landed (dequant group)
   uint64_t* bar_vready = bars + 10;   // V^T of a tile in shared memory (dequant group)
-  uint64_t* bar_pready = bars + 11;   // P^T and any O^T rescale of a tile done (softmax group)
-  uint64_t* bar_qk = bars + 12;       // [2] S^T buffer b written (MMA commit); its tile's R_k is in tensor memory
-  uint64_t* bar_pv = bars + 14;       // P.V of a tile completed (MMA commit)
+  uint64_t* bar_pready = bars + 11;   // [2] P^T of tile k (buffer k & 1) and any O^T rescale done (softmax group)
+  uint64_t* bar_qk = bars + 13;       // [2] S^T buffer b written (MMA commit); its tile's R_k is in tensor memory
+  uint64_t* bar_pv = bars + 15;       // [2] P.V of tile k completed (barrier k & 1; MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -730,10 +737,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     mbar_init(&bar_kready[0], kDqWarps);
     mbar_init(&bar_kready[1], kDqWarps);
     mbar_init(bar_vready, kDqWarps);
-    mbar_init(bar_pready, kSmWarps);
+    mbar_init(&bar_pready[0], kSmWarps);
+    mbar_init(&bar_pready[1], kSmWarps);
     mbar_init(&bar_qk[0], 1);
     mbar_init(&bar_qk[1], 1);
-    mbar_init(bar_pv, 1);
+    mbar_init(&bar_pv[0], 1);
+    mbar_init(&bar_pv[1], 1);
     fence_barrier_init();
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
@@ -902,63 +911,69 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   }
 
   // =========================== MMA warp =========================================
-  // Order of issue: QK(0), then per tile k: QK(k+1) once its K tile is ready, P.V(k)
-  // once its V^T and P^T are ready.
+  // Order of issue: QK(0), then per tile k the pair QK(k+1) (once its K tile is ready) and
+  // P.V(k) (once its V^T and P^T are ready), whichever is ready first.  Either order keeps
+  // QK(k+1) behind P.V(k-1), which follows the softmax of tile k-1 (the last reader of the
+  // S^T buffer that QK(k+1) writes).
   if (warp == kMmaWarp) {
     const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
     const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE5M2, true, true);
     const uint64_t dq0 = smem_desc_kmajor(smem_u32(smem + kOffQhat), kQLbo, kQSbo);
     const uint64_t dv0 = smem_desc_mnmajor(smem_u32(smem + kOffVt), kVtLbo, kVtSbo);
     const uint64_t dp0 = smem_desc_mnmajor(smem_u32(smem + kOffPt), kPtLbo, kPtSbo);
-    TileIter cur = it, nxt = it;
-    bool has_next = nxt.next();
-    int k = 0;
     // the last commit issued: it arrives once every MMA issued before it has completed
     uint64_t* last_bar = nullptr;
     uint32_t last_par = 0;
-    for (int kk = 0;; ++kk) {
-      if (*abort_word()) break;  // another role gave up: issue nothing more
-      // QK^T of tile kk (kk = 0 before the loop proper, then kk = k + 1)
-      if (kk == 0 || has_next) {
-        const int q = kk;
-        const TileIter& qt = kk == 0 ? cur : nxt;
-        if (!wait_or_flag(&bar_kready[q & 1], (q >> 1) & 1, p, aborted)) break;
-        tc_fence_after();
-        const uint32_t bq = q & 1;
-        const uint64_t dq = dq0 + (uint64_t)(((qt.seg & 1) * kQhatBytes) >> 4);
+    auto issue_qk = [&](int q, const TileIter& qt) {
+      tc_fence_after();
+      const uint32_t bq = q & 1;
+      const uint64_t dq = dq0 + (uint64_t)(((qt.seg & 1) * kQhatBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kDqk / 32; ++ks)
-          umma_f8_ts_warp(tmem + kColS + 32 * bq, tmem + kColA + kColsA * bq + 8 * ks,
-                          dq + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
-        umma_commit_warp(&bar_qk[bq]);
-        last_bar = &bar_qk[bq];
-        last_par = (uint32_t)(q >> 1) & 1u;
-        if (qt.last) {  // the segment's Qhat buffer may be refilled
-          umma_commit_warp(&bar_qfree[qt.seg & 1]);
-          last_bar = &bar_qfree[qt.seg & 1];
-          last_par = (uint32_t)(qt.seg >> 1) & 1u;
-        }
+      for (int ks = 0; ks < kDqk / 32; ++ks)
+        umma_f8_ts_warp(tmem + kColS + 32 * bq, tmem + kColA + kColsA * bq + 8 * ks,
+                        dq + (uint64_t)((ks * 2 * kQLbo) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+      umma_commit_warp(&bar_qk[bq]);
+      last_bar = &bar_qk[bq];
+      last_par = (uint32_t)(q >> 1) & 1u;
+      if (qt.last) {  // the segment's Qhat buffer may be refilled
+        umma_commit_warp(&bar_qfree[qt.seg & 1]);
+        last_bar = &bar_qfree[qt.seg & 1];
+        last_par = (uint32_t)(qt.seg >> 1) & 1u;
       }
-      if (kk == 0) continue;
-      // P.V of tile k
-      if (!wait_or_flag(bar_vready, k & 1, p, aborted)) break;
-      if (!wait_or_flag(bar_pready, k & 1, p, aborted)) break;
+    };
+    auto issue_pv = [&](int k, bool seg_first) {
       tc_fence_after();
       const uint64_t dp = dp0 + (uint64_t)(((k & 1) * kPtBytes) >> 4);
-      const bool seg_first = cur.first;
 #pragma unroll
       for (int js = 0; js < kTile / 32; ++js)
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk)
           umma_f8_ss_warp(tmem + kColO + 32 * blk, dv0 + (uint64_t)((blk * kVtBlock + js * 4 * kVtLbo) >> 4),
                           dp + (uint64_t)((js * 4 * kPtLbo) >> 4), idesc_pv, (js > 0 || !seg_first) ? 1u : 0u);
-      umma_commit_warp(bar_pv);
-      last_bar = bar_pv;
-      last_par = (uint32_t)k & 1u;
-      if (!has_next) break;
-      cur = nxt;
-      has_next = nxt.next();
-      ++k;
+      umma_commit_warp(&bar_pv[k & 1]);
+      last_bar = &bar_pv[k & 1];
+      last_par = (uint32_t)(k >> 1) & 1u;
+    };
+    TileIter cur = it, nxt = it;  // tiles k and k+1
+    bool has_next = nxt.next();
+    if (!*abort_word() && wait_or_flag(&bar_kready[0], 0, p, aborted)) {
+      issue_qk(0, cur);
+      for (int k = 0;; ++k) {
+        bool qk_todo = has_next, pv_todo = true;
+        if (*abort_word()) break;
+        if (has_next) {
+          if (!wait_or_flag(&bar_kready[(k + 1) & 1], ((k + 1) >> 1) & 1, p, aborted)) break;
+          issue_qk(k + 1, nxt);
+          qk_todo = false;
+        }
+        if (!wait_or_flag(bar_vready, k & 1, p, aborted)) break;
+        if (!wait_or_flag(&bar_pready[k & 1], (k >> 1) & 1, p, aborted)) break;
+        issue_pv(k, cur.first);
+        pv_todo = false;
+        if (qk_todo || pv_todo || !has_next) break;
+        cur = nxt;
+        has_next = nxt.next();
+      }
     }
     // The other groups are done with tensor memory, and every MMA has completed: in a normal
     // run the softmax group waited for each segment's last P.V; after an abort the last
@@ -1008,14 +1023,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     do {
       has_next = it.next();  // it: tile k+1 from here on (the V^T step below needs only k)
       if (has_next) {
-        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed:
-        // for k >= 2 that is implied by the completion of P.V of tile k-2, which the MMA warp issued
-        // after QK^T of tile k-1 and which this group waited for in the previous iteration ----
+        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed ----
         const int s1 = (k + 1) % kStages;
         const bool new_seg = it.first && gtid < kHeads;
         const float chv = new_seg ? p.ws.qch[it.b * kHeads + gtid] : 0.f;
         wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
-        if (k == 1) wait_or_flag(&bar_qk[0], 0, p, aborted);
+        if (k >= 1) wait_or_flag(&bar_qk[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
         if (new_seg) chs[(it.seg & 3) * kHeads + gtid] = chv;
         tc_fence_after();
         // the reference of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3,
@@ -1033,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         }
       }
       // ---- V^T of tile k (P.V of tile k-1, which read V^T, must have completed) ----
-      if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
+      if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
       tc_fence_after();
       {
         const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
@@ -1085,6 +1098,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       // S^T and the tile's reference exponent R_k (stored by the dequant group before the K
       // tile that QK^T read was declared ready; the same value in every lane)
       wait_or_flag(&bar_qk[k & 1], (k >> 1) & 1, p, aborted);
+      // The P^T buffer written below (k & 1) was last read by P.V of tile k-2, which the MMA
+      // warp issued before QK^T of tile k: the commit that signalled S^T of tile k covers it.
       tc_fence_after();
       int Rk;
       float s2[16];
@@ -1207,10 +1222,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         *reinterpret_cast<uint4*>(prow) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
         *reinterpret_cast<uint4*>(prow + kPtSbo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
       }
-      // ---- P.V of tile k-1 must be complete: O^T rescale below, and the phase of pready ----
-      if (k > 0) wait_or_flag(bar_pv, (k - 1) & 1, p, aborted);
-      tc_fence_after();
+      // ---- O^T rescale, once P.V of tile k-1 completed ----
       if (resc) {
+        if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
+        tc_fence_after();
         const float rs = exp2i(R - Rnew);
         // eight columns at a time (column 8q + i holds head (8q + i) % 16): few live registers
 #pragma unroll 1
@@ -1232,7 +1247,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       fence_proxy_async_smem();  // P^T is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pready);
+      if (lane == 0) mbar_arrive(&bar_pready[k & 1]);
       if (it.last) {
         // ---- segment epilogue: l over the segment, then O = (hi + lo) * 2^-kHead * 2^(R-127) / l ----
         float* lw = reinterpret_cast<float*>(smem + kOffLw);      // [16 heads][4 quarters]
@@ -1251,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           ofac[h] = os / L;
         }
         named_sync(kBarSm, kSmThreads);
-        wait_or_flag(bar_pv, k & 1, p, aborted);
+        wait_or_flag(&bar_pv[k & 1], (k >> 1) & 1, p, aborted);
         tc_fence_after();
         float of[16];
 #pragma unroll
