@@ -81,13 +81,14 @@ constexpr int kTokWarps = kDqWarps + kSmWarps;
 constexpr int kTokThreads = kTokWarps * 32;
 // Warp roles, in warp-index order (lower indices are favoured by the issue
 // schedulers, so the latency-critical roles come first): MMA issue, producer,
-// softmax group, dequant group.  A warp reaches tensor-memory lanes
+// softmax group, dequant group, tile references.  A warp reaches tensor-memory lanes
 // 32*(warp % 4)..+31; both groups cover every quarter.
 constexpr int kMmaWarp = 0;                  // tcgen05.mma issue (also allocates tensor memory)
 constexpr int kProdWarp = 1;                 // bulk async copies
 constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..5
 constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 6..17
-constexpr int kThreads = (kTokWarps + 2) * 32;
+constexpr int kRefWarp = kDqWarp0 + kDqWarps;   // tile reference exponents: warp 18
+constexpr int kThreads = (kTokWarps + 3) * 32;
 constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 constexpr int kPartSmemSeqs = 8192;  // the partition kernel keeps ipc in shared memory up to this batch
 
@@ -138,10 +139,13 @@ constexpr int kMaxRowsPerQuery = 1 << 20;
 constexpr int kStagePackedBytes = kTile * kPacked;                   // 36864
 constexpr int kStageScaleBytes = 2432;                               // >= 128*18 + 32, mult of 16
 constexpr int kStageBytes = kStagePackedBytes + kStageScaleBytes;    // 39296
-// The last word of a stage's scale area holds the offset (0..15) at which the tile's first
-// scale byte landed (written by the producer before the stage's copies are announced).
+// The scale bytes of a tile land in the first 16 + 128*18 bytes of the scale area.  The last
+// word holds the offset (0..15) at which the tile's first scale byte landed (written by the
+// producer before the stage's copies are announced); the word before it the tile's reference
+// exponent R (written by the reference warp once the stage has landed).
 constexpr int kStageMisOff = kStagePackedBytes + kStageScaleBytes - 4;
-static_assert(kStageScaleBytes - 4 >= 16 + ((kTile * kNScale + 15) / 16) * 16, "misalignment slot");
+constexpr int kStageRefOff = kStageMisOff - 4;
+static_assert(kStageRefOff >= kStagePackedBytes + 16 + ((kTile * kNScale + 15) / 16) * 16, "stage spare words");
 constexpr int kQhatBytes = 32 * kDqk;                                // 18432: e4m3 hi + lo query parts
 
 // Tensor memory (32-bit columns, lane = token of the tile / row of M):
@@ -191,7 +195,7 @@ constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230
 constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136: tensor-memory address
 constexpr int kOffAbort = kOffTmem + 4;                                   // abort word (bounded waits)
 constexpr int kOffBar = kOffTmem + 16;                                    // 231152
-constexpr int kNumBars = 17;
+constexpr int kNumBars = 20;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231288
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
@@ -618,13 +622,9 @@ __device__ __forceinline__ int next_reference(int T, int r_prev, int r_max, bool
 // further below are zero.  Tokens past the tile are zero.  Token t = this thread's lane of
 // the quarter; part p converts the consecutive blocks 6p .. 6p+5, two per step (the next
 // pair's bytes are loaded while this pair is converted; one 16-column store per pair).
-// Every dequant thread first takes the largest scale byte of its blocks; the group decides
-// R behind a barrier of the whole dequant group, which also orders every part's V^T copy of
-// the previous tile, read from the K buffer about to be overwritten, before any part
-// overwrites it.  Part 0 stores R in tensor-memory column r_col for the softmax group.
-// Returns R.
-__device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, int part, int q4, uint32_t a_lane,
-                                              uint32_t r_col, int* tq, int r_prev, int r_max, bool seg_first) {
+// Part 0 stores R in tensor-memory column r_col for the softmax group.
+__device__ __forceinline__ void k_tile_to_tmem(const uint8_t* st, int n, int t, int part, uint32_t a_lane,
+                                               uint32_t r_col, int R) {
   const bool valid = t < n;
   // where the tile's first scale byte landed (0..15): the producer's note in the stage, masked
   // so that a stage that never landed (a wait that gave up) is still read in bounds
@@ -634,25 +634,6 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, i
   static_assert(kNScale % kDqParts == 0 && kNb % 2 == 0, "pairs of blocks per part");
   const int b0 = part * kNb;
   const uint8_t* sp = sb + b0;
-  int m = 0;
-  if (valid) {
-#pragma unroll
-    for (int j = 0; j < kNb; ++j) m = max(m, (int)sp[j]);
-  }
-  // Within a segment the reference usually stays: T_k in [r_prev - kRefSlack, r_prev] keeps it,
-  // and two reducing barriers (every block at most r_prev; some block at least r_prev -
-  // kRefSlack) decide that without exchanging maxima.  Otherwise the warps' maxima meet in tq.
-  int R = r_prev;
-  if (seg_first || !named_sync_and(kBarDqTile, kDqThreads, m <= r_prev) ||
-      !named_sync_or(kBarDqTile, kDqThreads, m >= r_prev - kRefSlack)) {
-    m = (int)__reduce_max_sync(0xffffffffu, (unsigned)m);
-    if ((t & 31) == 0) tq[part * 4 + q4] = m;
-    named_sync(kBarDqTile, kDqThreads);
-    int T = 0;
-#pragma unroll
-    for (int i = 0; i < kDqWarps; ++i) T = max(T, tq[i]);
-    R = next_reference(T, r_prev, r_max, seg_first);
-  }
   if (part == 0) {
     const uint32_t rv[1] = {(uint32_t)R};
     tmem_st1(r_col, rv);
@@ -675,7 +656,6 @@ __device__ __forceinline__ int k_tile_to_tmem(const uint8_t* st, int n, int t, i
     chunk_to_e5m2(xb, (uint32_t)max(tb + sbias, 0) * 0x04000400u, *reinterpret_cast<uint32_t(*)[8]>(&e[8]));
     tmem_st16(a_lane + 8 * (b0 + j), e);
   }
-  return R;
 }
 
 // Maximum (kMax) or sum over the 32 lanes of sixteen per-lane values; lane L ends
@@ -712,6 +692,55 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
   return kMax ? fmaxf(x, r1) : x + r1;
 }
 
+// Reference warp of mla_split_kernel (out of line: its registers stay apart from the other
+// roles').  It walks the tiles in the producer's order: once a stage has landed, the warp
+// takes the tile's largest scale byte T over its tokens and the tile's reference exponent R
+// (next_reference), leaves R in the stage and signals the dequant group.
+__device__ __noinline__ void reference_warp(uint8_t* smem, uint64_t* bar_full, uint64_t* bar_tready, TileIter it,
+                                            uint64_t timeout_ns, int* status, int lane) {
+  int r_prev = 0, r_max = 0;  // reference of the last tile, largest of its segment so far
+  for (int k = 0;; ++k) {
+    const int s = k % kStages;
+    if (*abort_word()) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar_full[s], (uint32_t)(k / kStages) & 1u, timeout_ns))) {
+      if (lane == 0) flag_timeout(status);
+      break;
+    }
+    uint8_t* st = smem + kOffStages + s * kStageBytes;
+    const int lo = *reinterpret_cast<const int*>(st + kStageMisOff) & 15;
+    const int hi = lo + it.n * kNScale;  // the tile's scale bytes are [lo, hi) of the scale area
+    uint32_t acc = 0;                    // maxima of the even and the odd bytes, as 16-bit lanes
+    for (int c = lane; 16 * c < hi; c += 32) {
+      const uint4 w4 = *reinterpret_cast<const uint4*>(st + kStagePackedBytes + 16 * c);
+      const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int o = 16 * c + 4 * i;
+        uint32_t m = 0xFFFFFFFFu;
+        if (o < lo || o + 4 > hi) {  // a word at either end: only bytes in [lo, hi) count
+          m = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (o + b >= lo && o + b < hi) m |= 0xFFu << (8 * b);
+        }
+        const uint32_t v = ws[i] & m;
+        acc = vmax_u16x2(acc, prmt(v, 0u, 0x4240u));
+        acc = vmax_u16x2(acc, prmt(v, 0u, 0x4341u));
+      }
+    }
+    const int T = (int)__reduce_max_sync(0xffffffffu, max(acc & 0xFFFFu, acc >> 16));
+    const int R = next_reference(T, r_prev, r_max, it.first);
+    r_max = it.first ? R : max(r_max, R);
+    r_prev = R;
+    __syncwarp();
+    if (lane == 0) {
+      *reinterpret_cast<int*>(st + kStageRefOff) = R;
+      mbar_arrive(&bar_tready[s]);
+    }
+    if (!it.next()) break;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
   uint8_t* smem = dyn_smem;
   const int tid = threadIdx.x;
@@ -723,10 +752,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   uint64_t* bar_empty = bars + 3;     // [3] stage consumed (dequant group)
   uint64_t* bar_qfree = bars + 6;     // [2] Qhat buffer b read by the last QK^T of its segment (MMA commit)
   uint64_t* bar_kready = bars + 8;    // [2] K tile in tensor-memory buffer b ready, its Qhat landed (dequant group)
-  uint64_t* bar_vready = bars + 10;   // V^T of a tile in shared memory (dequant group)
-  uint64_t* bar_pready = bars + 11;   // [2] P^T of tile k (buffer k & 1) and any O^T rescale done (softmax group)
+  // (slot 10 unused)
+  uint64_t* bar_pready = bars + 11;   // [2] P^T and V^T of tile k and any O^T rescale done (softmax group)
   uint64_t* bar_qk = bars + 13;       // [2] S^T buffer b written (MMA commit); its tile's R_k is in tensor memory
   uint64_t* bar_pv = bars + 15;       // [2] P.V of tile k completed (barrier k & 1; MMA commit)
+  uint64_t* bar_tready = bars + 17;   // [3] stage landed and its tile's reference exponent written (reference warp)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -736,13 +766,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     mbar_init(&bar_qfree[1], 1);
     mbar_init(&bar_kready[0], kDqWarps);
     mbar_init(&bar_kready[1], kDqWarps);
-    mbar_init(bar_vready, kDqWarps);
     mbar_init(&bar_pready[0], kSmWarps);
     mbar_init(&bar_pready[1], kSmWarps);
     mbar_init(&bar_qk[0], 1);
     mbar_init(&bar_qk[1], 1);
     mbar_init(&bar_pv[0], 1);
     mbar_init(&bar_pv[1], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar_tready[s], 1);
     fence_barrier_init();
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
@@ -910,11 +940,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     return;
   }
 
+  // =========================== reference warp ===================================
+  if (warp == kRefWarp) {
+    reference_warp(smem, bar_full, bar_tready, it, p.timeout_ns, &p.ws.meta[kMetaStatus], lane);
+    return;
+  }
+
   // =========================== MMA warp =========================================
-  // Order of issue: QK(0), then per tile k the pair QK(k+1) (once its K tile is ready) and
-  // P.V(k) (once its V^T and P^T are ready), whichever is ready first.  Either order keeps
-  // QK(k+1) behind P.V(k-1), which follows the softmax of tile k-1 (the last reader of the
-  // S^T buffer that QK(k+1) writes).
+  // Order of issue: QK(0), then per tile k: QK(k+1) once its K tile is ready, P.V(k) once the
+  // softmax group has written its P^T and V^T.  QK(k+1) follows P.V(k-1), which follows the softmax of tile k-1
+  // (the last reader of the S^T buffer that QK(k+1) writes).
   if (warp == kMmaWarp) {
     const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
     const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE5M2, true, true);
@@ -966,7 +1001,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
           issue_qk(k + 1, nxt);
           qk_todo = false;
         }
-        if (!wait_or_flag(bar_vready, k & 1, p, aborted)) break;
         if (!wait_or_flag(&bar_pready[k & 1], (k >> 1) & 1, p, aborted)) break;
         issue_pv(k, cur.first);
         pv_todo = false;
@@ -992,25 +1026,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 
   if (warp >= kDqWarp0) {
     // ======================= dequant group (warps 6..17) ========================
-    // Iteration k: K tile k+1 -> tensor memory; V^T of tile k -> shared memory.
-    // Warp (q4, part) owns tokens 32*q4.., K blocks 6*part .. 6*part+5 and V blocks
-    // b == part (mod kDqParts).
+    // Iteration k: K tile k+1 -> tensor memory.  Warp (q4, part) owns tokens 32*q4.. and
+    // K blocks 6*part .. 6*part+5.
     const int dwarp = warp - kDqWarp0;  // 0..7
     const int part = dwarp >> 2;
     const int gtid = tid - kDqWarp0 * 32;  // 0..383
-    uint8_t* vt = smem + kOffVt;
     // Segment j's score factors go to slot j % 4 of the ring, read by the softmax of its
     // tiles; slot j % 4 was last read by segment j - 4, whose tiles precede tile k - 2 when
-    // segment j starts at tile k + 1, and P.V of tile k - 2 was waited for in iteration k - 1.
+    // segment j starts at tile k + 1, and the softmax group finished them before it signalled
+    // tile k - 1 (waited for below).
     float* chs = reinterpret_cast<float*>(smem + kOffCh);
     // prologue: tile 0 (a segment start)
     if (gtid < kHeads) chs[(it.seg & 3) * kHeads + gtid] = p.ws.qch[it.b * kHeads + gtid];
+    // a stage is converted once it landed and the producer warp wrote its reference exponent
     wait_or_flag(&bar_full[0], 0, p, aborted);
-    int* tq = reinterpret_cast<int*>(smem + kOffStq);  // [2 tile parities][12 dequant warps]
-    // reference exponent of the last converted tile and the largest of its segment
-    int r_ref = k_tile_to_tmem(smem + kOffStages, it.n, t, part, q4, t_lane + kColA, t_lane + kColSt, tq, 0, 0,
-                               true);
-    int r_max = r_ref;
+    wait_or_flag(&bar_tready[0], 0, p, aborted);
+    k_tile_to_tmem(smem + kOffStages, it.n, t, part, t_lane + kColA, t_lane + kColSt,
+                   *reinterpret_cast<const int*>(smem + kOffStages + kStageRefOff));
     tc_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -1018,67 +1050,30 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
       mbar_arrive(&bar_kready[0]);
       mbar_arrive(&bar_empty[0]);
     }
-    int k = 0;
-    bool has_next;
-    do {
-      has_next = it.next();  // it: tile k+1 from here on (the V^T step below needs only k)
-      if (has_next) {
-        // ---- K tile k+1 -> tensor-memory buffer (k+1)&1, once QK^T of tile k-1 (which read it) completed ----
-        const int s1 = (k + 1) % kStages;
-        const bool new_seg = it.first && gtid < kHeads;
-        const float chv = new_seg ? p.ws.qch[it.b * kHeads + gtid] : 0.f;
-        wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
-        if (k >= 1) wait_or_flag(&bar_qk[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
-        if (new_seg) chs[(it.seg & 3) * kHeads + gtid] = chv;
-        tc_fence_after();
-        // the reference of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3,
-        // which finished before P.V of tile k-3 (waited for two iterations ago)
-        r_ref = k_tile_to_tmem(smem + kOffStages + s1 * kStageBytes, it.n, t, part, q4,
-                               t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
-                               tq + ((k + 1) & 1) * kDqWarps, r_ref, r_max, it.first);
-        r_max = it.first ? r_ref : max(r_max, r_ref);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar_kready[(k + 1) & 1]);
-          mbar_arrive(&bar_empty[s1]);
-        }
-      }
-      // ---- V^T of tile k (P.V of tile k-1, which read V^T, must have completed) ----
-      if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
+    for (int k = 0; it.next(); ++k) {  // it: tile k+1
+      // ---- K tile k+1 -> tensor-memory buffer (k+1)&1.  The buffer held tile k-1, read by its
+      // QK^T and by the softmax group's V^T copy; both are done once the softmax group signalled
+      // tile k-1 (it waited for that QK^T first) ----
+      const int s1 = (k + 1) % kStages;
+      const bool new_seg = it.first && gtid < kHeads;
+      const float chv = new_seg ? p.ws.qch[it.b * kHeads + gtid] : 0.f;
+      wait_or_flag(&bar_full[s1], ((k + 1) / kStages) & 1, p, aborted);
+      wait_or_flag(&bar_tready[s1], ((k + 1) / kStages) & 1, p, aborted);
+      if (k >= 1) wait_or_flag(&bar_pready[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
+      if (new_seg) chs[(it.seg & 3) * kHeads + gtid] = chv;
       tc_fence_after();
-      {
-        const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
-        uint8_t* vrow = vt + (t >> 3) * kVtLbo + (t & 7) * 16;
-        // V blocks b == part (mod kDqParts), b < 16, in batches of three
-        constexpr int kNv = (kDv / 32 + kDqParts - 1) / kDqParts;
-#pragma unroll
-        for (int hb = 0; hb < (kNv + 2) / 3; ++hb) {
-          uint32_t e[3][8];
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const int b = part + kDqParts * (3 * hb + j);
-            if (3 * hb + j < kNv && b < kDv / 32) tmem_ld8_nowait(acol + 8 * b, e[j]);
-          }
-          tc_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const int b = part + kDqParts * (3 * hb + j);  // dims 32b .. 32b+31
-            if (3 * hb + j >= kNv) continue;
-            if (b >= kDv / 32) continue;
-            uint8_t* d0 = vrow + (b >> 2) * kVtBlock + 2 * (b & 3) * kVtSbo;
-            *reinterpret_cast<uint4*>(d0) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
-            *reinterpret_cast<uint4*>(d0 + kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
-          }
-        }
-      }
-      fence_proxy_async_smem();  // V^T is read by the tensor cores
+      // the reference of tile k+1 goes to column (k+1) % 4, last read by the softmax of tile k-3
+      const uint8_t* st = smem + kOffStages + s1 * kStageBytes;
+      k_tile_to_tmem(st, it.n, t, part, t_lane + kColA + kColsA * ((k + 1) & 1), t_lane + kColSt + ((k + 1) & 3),
+                     *reinterpret_cast<const int*>(st + kStageRefOff));
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_vready);
-      ++k;
-    } while (has_next);
+      if (lane == 0) {
+        mbar_arrive(&bar_kready[(k + 1) & 1]);
+        mbar_arrive(&bar_empty[s1]);
+      }
+    }
   } else {
     // ======================= softmax group (warps 2..5) =========================
     // Warp q4 owns tokens 32*q4.. of each tile and all 16 heads; lane L keeps the
@@ -1222,10 +1217,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         *reinterpret_cast<uint4*>(prow) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
         *reinterpret_cast<uint4*>(prow + kPtSbo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
       }
-      // ---- O^T rescale, once P.V of tile k-1 completed ----
+      // ---- P.V of tile k-1 must be complete: O^T rescale and V^T below ----
+      if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
+      tc_fence_after();
       if (resc) {
-        if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
-        tc_fence_after();
         const float rs = exp2i(R - Rnew);
         // eight columns at a time (column 8q + i holds head (8q + i) % 16): few live registers
 #pragma unroll 1
@@ -1244,7 +1239,25 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         tc_wait_st();
       }
       R = Rnew;
-      fence_proxy_async_smem();  // P^T is read by the tensor cores
+      // ---- V^T of tile k: this thread's token, all 512 dims, from the K tile in tensor memory ----
+      {
+        const uint32_t acol = t_lane + kColA + kColsA * (k & 1);
+        uint8_t* vrow = smem + kOffVt + (t >> 3) * kVtLbo + (t & 7) * 16;
+#pragma unroll 1
+        for (int b4 = 0; b4 < kDv / 32; b4 += 4) {  // blocks b4 .. b4+3 = dims 32*b4 .. 32*b4+127
+          uint32_t e[4][8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tmem_ld8_nowait(acol + 8 * (b4 + j), e[j]);
+          tc_wait_ld();
+          uint8_t* d = vrow + (b4 >> 2) * kVtBlock;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<uint4*>(d + 2 * j * kVtSbo) = make_uint4(e[j][0], e[j][1], e[j][2], e[j][3]);
+            *reinterpret_cast<uint4*>(d + (2 * j + 1) * kVtSbo) = make_uint4(e[j][4], e[j][5], e[j][6], e[j][7]);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // P^T and V^T are read by the tensor cores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pready[k & 1]);

@@ -100,6 +100,12 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
       : "memory");
   return r != 0;
 }
+// Lane-wise maximum of two pairs of unsigned 16-bit values.
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
