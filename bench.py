@@ -53,21 +53,21 @@ def _peaks():
 
 def kernel_source_sha1():
     h = hashlib.sha1()
-    for f in ("mla_kernels.cuh", "ptx.cuh", "mla_api.cu"):
+    for f in ("mla_kernels.cuh", "mla_fp8_kernel.cuh", "ptx.cuh", "mla_api.cu"):
         with open(os.path.join(ROOT, "mla_decode_attention_mxfp4_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def _traffic_per_launch(workload):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+def _traffic_per_launch(workload, kernel="mla_split_kernel"):
+    """DRAM bytes per launch of a split kernel from the committed ncu summary,
     only if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get("mla_split_kernel", {}).get(workload)
+    e = d.get(kernel, {}).get(workload)
     if not e or e.get("source_sha1") != kernel_source_sha1():
         return None
     return e.get("dram_bytes_per_launch")
@@ -408,12 +408,13 @@ class GeneralWorkload(DeviceWorkload):
     def roofline(self, split_ms, peak, peak_src, workload):
         r = DeviceWorkload.roofline(self, split_ms, peak, peak_src, workload)
         r["kernel"] = "mla_split_fp8_kernel" if self.form == "fp8" else "mla_split_kernel"
-        r["traffic"] = None
+        r["traffic"] = _traffic_per_launch(workload, r["kernel"])
         return r
 
 
-NUMERICS = ("K/V as e5m2 (exact e2m1*2^k per token, 13 binades of headroom), query and P as two e4m3 "
-            "terms each, tcgen05 f8f6f4 MMAs with fp32 accumulation, fp32 softmax and merge, bf16 out")
+NUMERICS = ("K/V as e5m2 against a per-tile reference exponent (exact for blocks within 27 binades of "
+            "the tile's largest scale), query as two e4m3 terms, P*2^11 as two e5m2 terms, tcgen05 f8f6f4 "
+            "MMAs with fp32 accumulation, fp32 softmax and merge, bf16 out")
 
 
 def run_native(args):
