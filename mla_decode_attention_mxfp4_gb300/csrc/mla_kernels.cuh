@@ -25,11 +25,13 @@
 //                   buffers at a segment start);
 //       warps 2..5  softmax group, one warp per tensor-memory lane quarter (32
 //                   tokens), all 16 heads: online softmax of S^T, P as e5m2 hi + lo
-//                   parts, rescaling of the O^T accumulator, segment epilogue;
-//       warps 6..17 dequant group, three warps per lane quarter: the tile's
-//                   reference exponent, the K tile as e5m2 into tensor memory (A operand of
-//                   QK^T, double-buffered), V^T as e5m2 into shared memory, the
-//                   score factors at a segment start.
+//                   parts, rescaling of the O^T accumulator, V^T of the tile from the
+//                   K tile in tensor memory into shared memory, segment epilogue;
+//       warps 6..17 dequant group, three warps per lane quarter: the K tile as e5m2
+//                   into tensor memory (A operand of QK^T, double-buffered), the
+//                   score factors at a segment start;
+//       warp 18     reference warp: each landed tile's largest scale byte and its
+//                   reference exponent, handed to the dequant group with the stage.
 //     QK^T (S^T[128 tokens][32] = K . Qhat^T, hi and lo query parts stacked as N)
 //     and P.V (O^T[512][32] += V^T . P^T) run on tcgen05 kind::f8f6f4 with fp32
 //     accumulators in tensor memory.  The groups hand tiles to each other through
@@ -186,23 +188,20 @@ constexpr int kOffQhat = kOffStages + kStages * kStageBytes;              // 117
 constexpr int kOffVt = kOffQhat + 2 * kQhatBytes;                         // 154752
 constexpr int kOffPt = kOffVt + 4 * kVtBlock;                             // 220288
 constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                           // 228480: [2][16 heads][4 quarters]
-constexpr int kOffRw = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: (unused, 32 bytes)
-constexpr int kOffCh = kOffRw + 32;                                       // 229024: [4][16] score factors
-constexpr int kOffLw = kOffCh + 4 * kHeads * 4;                           // 229280: [16 heads][4 quarters]
-constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229536: [16] output factors
-constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229600: [4 warps][16 m, 16 alpha]
-constexpr int kOffStq = kOffMst + 4 * 2 * kHeads * 4;                     // 230112: [2][12] scale maxima per dequant warp
-constexpr int kOffTmem = kOffStq + 2 * kTile * 4;                         // 231136: tensor-memory address
+constexpr int kOffCh = kOffHmax + 2 * 4 * kHeads * 4;                     // 228992: [4][16] score factors
+constexpr int kOffLw = kOffCh + 4 * kHeads * 4;                           // 229248: [16 heads][4 quarters]
+constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                        // 229504: [16] output factors
+constexpr int kOffMst = kOffMlast + kHeads * 4;                           // 229568: [4 warps][16 m, 16 alpha]
+constexpr int kOffTmem = kOffMst + 4 * 2 * kHeads * 4;                    // 230080: tensor-memory address
 constexpr int kOffAbort = kOffTmem + 4;                                   // abort word (bounded waits)
-constexpr int kOffBar = kOffTmem + 16;                                    // 231152
+constexpr int kOffBar = kOffTmem + 16;                                    // 230096
 constexpr int kNumBars = 20;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 231288
+constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 230256
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
 constexpr uint32_t kBarSm = 1;     // named barrier of the softmax group
 constexpr uint32_t kBarAll = 2;    // dequant + softmax groups + MMA warp
-constexpr uint32_t kBarDqTile = 3; // dequant group: the tile's scale maxima (once per tile)
 
 struct SplitParams {
   const uint8_t* kv;

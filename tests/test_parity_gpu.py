@@ -308,10 +308,10 @@ def test_scale_extremes_and_query_range():
 
 def test_running_maxima_move_late_in_a_sequence():
     """A token far into a sequence whose scale bytes are raised: its scores jump by far
-    more than the raise threshold and so does its token exponent, so the running maxima
-    move in the middle of a segment and the accumulator is rescaled (the full path of the
-    softmax statistics); a later block of tokens with raised exponents does the same for
-    the token-exponent maximum alone."""
+    more than the raise threshold and so does its tile's reference exponent, so the running
+    maxima move in the middle of a segment and the accumulator is rescaled (the full path of
+    the softmax statistics); a later block of tokens with raised exponents moves the tile
+    reference up and back down again."""
     d = MI.make_custom([1000, 700, 300], seed=71)
     s = d.kv_scale.clone().to(torch.int32)
     s[900] += 6                      # one late token 64x larger than the rest
