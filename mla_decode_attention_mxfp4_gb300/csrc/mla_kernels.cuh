@@ -196,7 +196,9 @@ constexpr int kOffTmem = kOffMst + 4 * 2 * kHeads * 4;                    // 230
 constexpr int kOffAbort = kOffTmem + 4;                                   // abort word (bounded waits)
 constexpr int kOffBar = kOffTmem + 16;                                    // 230096
 constexpr int kNumBars = 20;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8;                        // 230256
+constexpr int kOffPid = kOffBar + kNumBars * 8;                           // 230256: [16] page ids of a tile (producer)
+constexpr int kTilePidSlots = 16;
+constexpr int kSmemBytes = kOffPid + kTilePidSlots * 4;                   // 230320
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffVt % 16 == 0 && kOffPt % 16 == 0 && kOffQhat % 16 == 0, "operand alignment");
 
@@ -806,9 +808,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     // Paged layout: the run of the tile's tokens that starts at tile row i lies in one page:
     // `cnt` rows from physical row `row`.
     // Paged layout: the sequence's logical start and its first kv_indices entry are loaded
-    // once per segment; a tile's page ids (it touches at most kTilePages pages when
-    // page_size >= 16) are loaded together into registers, then both passes walk the runs.
-    constexpr int kTilePages = kTile / 16 + 1;
+    // once per segment; a tile's page ids (at most kTilePidSlots of them when page_size >= 9)
+    // are loaded together and kept in shared memory while one pass walks the runs.
+    int* pid_s = reinterpret_cast<int*>(smem + kOffPid);
     int seg_b = -1, seg_pos0 = 0, seg_ix0 = 0;
     int k = 0;
     if (!p.stall_producer) do {
@@ -845,9 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         // offset dst0 + (x - g0), dst0 = M + 18 i: the 16-byte chunks [c0, a1) by bulk copy when
         // source and destination agree modulo 16, the other bytes by plain loads.  At the tile's
         // own ends the bulk range may round outwards (the extra bytes land outside the tile's
-        // part of the area); between runs it rounds inwards.  Pass 1 does the plain loads and
-        // counts the bulk bytes; the stage is then announced with its byte count; pass 2
-        // issues the bulk copies.
+        // part of the area); between runs it rounds inwards.  One pass over the runs issues the
+        // plain loads and the bulk copies and counts the bulk bytes; the stage is announced with
+        // that count afterwards (the barrier's transaction count may run below zero until then,
+        // and the phase cannot complete before this thread's arrival).
         if (it.b != seg_b) {
           seg_b = it.b;
           seg_pos0 = p.ws.ipc[seg_b];
@@ -857,72 +860,54 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
         const int pos0 = it.t0 - seg_pos0;
         const int pg0 = pos0 / ps, off0 = pos0 - pg0 * ps;
         const int npg = (off0 + it.n + ps - 1) / ps;  // pages the tile touches
-        int pid[kTilePages];
-        const bool in_regs = npg <= kTilePages;
-        if (in_regs) {
-#pragma unroll
-          for (int u = 0; u < kTilePages; ++u) pid[u] = u < npg ? p.kv_indices[seg_ix0 + pg0 + u] : 0;
-#pragma unroll
-          for (int u = 0; u < kTilePages; ++u) {
-            if (u < npg && (pid[u] < 0 || pid[u] >= p.num_pages)) {  // clamped into the buffers, and flagged
-              atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
-              pid[u] = min(max(pid[u], 0), max(p.num_pages - 1, 0));
-            }
+        const bool in_smem = npg <= kTilePidSlots;
+        auto clamp_page = [&](int page) {  // an id outside the buffers is clamped into them, and flagged
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
+            page = min(max(page, 0), max(p.num_pages - 1, 0));
           }
-        }
-        // run u (u < npg): tile rows [i, i + cnt) from physical row `row`
-        auto run = [&](int u, int& i, int& cnt, long long& row) {
-          int page = 0;
-          if (in_regs) {
-#pragma unroll
-            for (int v = 0; v < kTilePages; ++v)
-              if (v == u) page = pid[v];
-          } else {
-            page = p.kv_indices[seg_ix0 + pg0 + u];
-            if (page < 0 || page >= p.num_pages) {
-              atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
-              page = min(max(page, 0), max(p.num_pages - 1, 0));
-            }
-          }
-          const int off = u == 0 ? off0 : 0;
-          i = u == 0 ? 0 : ps * u - off0;
-          cnt = min(ps - off, it.n - i);
-          row = (long long)page * ps + off;
+          return page;
         };
-        int i0, c0n;
-        long long row0;
-        run(0, i0, c0n, row0);
-        const int M = (int)((p.sc_mis + row0 * kNScale) & 15);
-        uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
-        for (int pass = 0; pass < 2; ++pass) {
-          for (int u = 0; u < npg; ++u) {
-            int i, cnt;
-            long long row;
-            run(u, i, cnt, row);
-            const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
-            const long long dst0 = M + (long long)i * kNScale;
-            long long c0 = g1, a1 = g1;  // no bulk range
-            if (((g0 - dst0) & 15) == 0) {
-              c0 = i == 0 ? (g0 & ~15LL) : ((g0 + 15) & ~15LL);
-              a1 = i + cnt == it.n ? ((g1 + 15) & ~15LL) : (g1 & ~15LL);
-              if (c0 < head16) c0 = head16;
-              if (a1 > scale_end16) a1 = scale_end16;
-              if (a1 < c0) a1 = c0;
-            }
-            if (pass == 0) {
-              for (long long x = g0; x < g1 && x < c0; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
-              for (long long x = (a1 > g0 ? a1 : g0); x < g1; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
-              bytes += (uint32_t)cnt * kPacked + (uint32_t)(a1 - c0);
-            } else {
-              bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
-              if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
-            }
+        if (in_smem) {
+          const int* src = p.kv_indices + seg_ix0 + pg0;
+          int u = 0;
+          for (; u + 4 <= npg; u += 4) {  // four loads in flight, then their stores
+            const int a0 = src[u], a1v = src[u + 1], a2 = src[u + 2], a3 = src[u + 3];
+            pid_s[u] = clamp_page(a0);
+            pid_s[u + 1] = clamp_page(a1v);
+            pid_s[u + 2] = clamp_page(a2);
+            pid_s[u + 3] = clamp_page(a3);
           }
-          if (pass == 0) {
-            *reinterpret_cast<int*>(st + kStageMisOff) = M;
-            mbar_arrive_expect_tx(&bar_full[s], bytes);
-          }
+          for (; u < npg; ++u) pid_s[u] = clamp_page(src[u]);
         }
+        int M = 0;
+        uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
+        for (int u = 0; u < npg; ++u) {
+          // run u: tile rows [i, i + cnt) from physical row `row`
+          const int page = in_smem ? pid_s[u] : clamp_page(p.kv_indices[seg_ix0 + pg0 + u]);
+          const int off = u == 0 ? off0 : 0;
+          const int i = u == 0 ? 0 : ps * u - off0;
+          const int cnt = min(ps - off, it.n - i);
+          const long long row = (long long)page * ps + off;
+          const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
+          if (u == 0) M = (int)(g0 & 15);
+          const long long dst0 = M + (long long)i * kNScale;
+          long long c0 = g1, a1 = g1;  // no bulk range
+          if (((g0 - dst0) & 15) == 0) {
+            c0 = i == 0 ? (g0 & ~15LL) : ((g0 + 15) & ~15LL);
+            a1 = i + cnt == it.n ? ((g1 + 15) & ~15LL) : (g1 & ~15LL);
+            if (c0 < head16) c0 = head16;
+            if (a1 > scale_end16) a1 = scale_end16;
+            if (a1 < c0) a1 = c0;
+          }
+          for (long long x = g0; x < g1 && x < c0; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+          for (long long x = (a1 > g0 ? a1 : g0); x < g1; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+          bytes += (uint32_t)cnt * kPacked + (uint32_t)(a1 - c0);
+          bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
+          if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+        }
+        *reinterpret_cast<int*>(st + kStageMisOff) = M;
+        mbar_arrive_expect_tx(&bar_full[s], bytes);
       }
       if (it.first)
         bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
