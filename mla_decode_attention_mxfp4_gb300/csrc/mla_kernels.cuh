@@ -932,8 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
 
   // =========================== MMA warp =========================================
   // Order of issue: QK(0), then per tile k: QK(k+1) once its K tile is ready, P.V(k) once the
-  // softmax group has written its P^T and V^T.  QK(k+1) follows P.V(k-1), which follows the softmax of tile k-1
-  // (the last reader of the S^T buffer that QK(k+1) writes).
+  // softmax group has written its P^T and V^T.  QK(k+1) follows P.V(k-1), which follows the
+  // softmax of tile k-1 (the last reader of the S^T buffer that QK(k+1) writes).
   if (warp == kMmaWarp) {
     const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE5M2, kFmtE4M3, false, false);
     const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE5M2, kFmtE5M2, true, true);
@@ -1012,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     // ======================= dequant group (warps 6..17) ========================
     // Iteration k: K tile k+1 -> tensor memory.  Warp (q4, part) owns tokens 32*q4.. and
     // K blocks 6*part .. 6*part+5.
-    const int dwarp = warp - kDqWarp0;  // 0..7
+    const int dwarp = warp - kDqWarp0;  // 0..11
     const int part = dwarp >> 2;
     const int gtid = tid - kDqWarp0 * 32;  // 0..383
     // Segment j's score factors go to slot j % 4 of the ring, read by the softmax of its
@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
     float* chs = reinterpret_cast<float*>(smem + kOffCh);
     // prologue: tile 0 (a segment start)
     if (gtid < kHeads) chs[(it.seg & 3) * kHeads + gtid] = p.ws.qch[it.b * kHeads + gtid];
-    // a stage is converted once it landed and the producer warp wrote its reference exponent
+    // a stage is converted once it landed and the reference warp wrote its reference exponent
     wait_or_flag(&bar_full[0], 0, p, aborted);
     wait_or_flag(&bar_tready[0], 0, p, aborted);
     k_tile_to_tmem(smem + kOffStages, it.n, t, part, t_lane + kColA, t_lane + kColSt,
