@@ -561,7 +561,9 @@ def run_native(args):
         "roofline": W.roofline(split_ms, peak, peak_src, args.workload),
         "e2e": {"value": whole_job_gbps(ws, W.nbytes, e2e_ms), "unit": "GB/s", "us_per_call": e2e_ms * 1e3,
                 "h2d_bytes_per_step": W.in_bytes + d.kv_indptr.numel() * 4,
-                "d2h_bytes_per_step": d.batch * 16 * 512 * 2},
+                "d2h_bytes_per_step": d.batch * 16 * 512 * 2,
+                "path": "HostDecoder: the kernels read q, kv_packed and kv_scale in place from pinned host "
+                        "memory (each byte crosses the host link once); kv_indptr copied in, out copied back"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "extra_workloads": extra,

@@ -249,6 +249,17 @@ int mla_decode_mxfp4_last_device_status(mla_stream_t stream, int* status);
  * that had one).  Safe to call at any time when no call is in flight. */
 void mla_decode_mxfp4_release(void);
 
+/* Device address of `host`, an address inside a page-locked host allocation that is
+ * mapped into the device's address space (cudaHostAlloc, cudaHostRegister with mapping;
+ * under unified addressing every page-locked allocation is), written to *device.  Passing
+ * that address as q, kv_packed or kv_scale to a decode entry point makes its kernels read
+ * the host buffer in place over the host link, with no copy into device memory first (the
+ * inputs are read once per call; kv_indptr, out and the workspace are better kept in device
+ * memory, as they are read or written many times).  The host buffer must stay allocated and
+ * unmodified until the call has completed on its stream.  Returns MLA_OK, MLA_ERR_NULL_PTR, or
+ * MLA_ERR_CUDA when `host` is not mapped page-locked memory (*device is then NULL). */
+int mla_host_device_pointer(const void* host, void** device);
+
 /* Human-readable name of an mla_status code. */
 const char* mla_status_string(int status);
 

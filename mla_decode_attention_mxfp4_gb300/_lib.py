@@ -82,12 +82,21 @@ def lib():
     L.mla_decode_mxfp4_release.argtypes = []
     L.mla_status_string.restype = ctypes.c_char_p
     L.mla_status_string.argtypes = [i]
+    L.mla_host_device_pointer.restype = i
+    L.mla_host_device_pointer.argtypes = [vp, ctypes.POINTER(vp)]
     _lib = L
     return L
 
 
 def status_string(code: int) -> str:
     return lib().mla_status_string(int(code)).decode()
+
+
+def host_device_pointer(host_ptr: int) -> tuple[int, int]:
+    """(status, device address) of a pointer into mapped page-locked host memory."""
+    out = ctypes.c_void_p(0)
+    rc = lib().mla_host_device_pointer(host_ptr, ctypes.byref(out))
+    return rc, (out.value or 0)
 
 
 # ---- raw C-ABI calls (integer device pointers) ---------------------------------------

@@ -159,8 +159,12 @@ def device_status(stream: torch.cuda.Stream | None = None, workspace: torch.Tens
 
 
 class HostDecoder:
-    """End-to-end decode from pinned host buffers: H2D copies, decode, D2H of the output.
+    """End-to-end decode from pinned host buffers, output copied back to a host tensor.
 
+    direct (default): the kernels read q, kv_packed and kv_scale in place from the pinned
+    host buffers (mla_host_device_pointer gives their device addresses; each byte crosses
+    the host link once, inside the decode); kv_indptr is copied to the device first.
+    Otherwise, or when an input is not pinned: H2D copies, decode, D2H of the output.
     Device buffers are allocated once for the largest shape seen.  The batch is cut into
     `chunks` groups of whole sequences with about equal KV rows; the copies of group c+1
     (on a copy stream) overlap the decode of group c (on the compute stream).  kv_indptr
@@ -169,12 +173,14 @@ class HostDecoder:
     non-decreasing sequence within the rows is sent as one group.
     """
 
-    def __init__(self, device="cuda", chunks: int = 4):
+    def __init__(self, device="cuda", chunks: int = 4, direct: bool = True):
         self.device = torch.device(device)
         self.stream = torch.cuda.Stream(self.device)
         self.copy_stream = torch.cuda.Stream(self.device)
         self.chunks = max(1, int(chunks))
+        self.direct = bool(direct)
         self._bufs = {}
+        self._ws = None
 
     def _buf(self, name, like: torch.Tensor):
         b = self._bufs.get(name)
@@ -204,7 +210,39 @@ class HostDecoder:
                 break
         return groups
 
+    def _device_address(self, t: torch.Tensor) -> int:
+        rc, addr = _lib.host_device_pointer(t.data_ptr())
+        if rc != _lib.MLA_OK or not addr:
+            raise _lib.MlaError(rc, "mla_host_device_pointer")
+        return addr
+
+    def _call_direct(self, q, kv_packed, kv_scale, kv_indptr, sm_scale, out_host):
+        B = q.shape[0]
+        if (q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[1] != NUM_HEADS or q.shape[2] != QK_DIM
+                or kv_packed.dtype != torch.uint8 or kv_packed.shape[-1] != PACKED
+                or kv_scale.dtype != torch.uint8 or kv_scale.shape[-1] != NSCALE
+                or kv_scale.numel() // NSCALE != kv_packed.numel() // PACKED
+                or kv_indptr.dtype != torch.int32 or kv_indptr.numel() != B + 1):
+            raise ValueError("host inputs: q bf16 [B,16,576], kv_packed uint8 [rows,288], "
+                             "kv_scale uint8 [rows,18], kv_indptr int32 [B+1]")
+        aq, akv, asc = (self._device_address(t) for t in (q, kv_packed, kv_scale))
+        dip, dout = self._buf("ip", kv_indptr), self._buf("out", out_host)
+        if self._ws is None or self._ws_batch < B:
+            self._ws, self._ws_batch = alloc_workspace(B, self.device), B
+        ms = self.stream
+        with torch.cuda.stream(ms):
+            dip.copy_(kv_indptr, non_blocking=True)
+            rc = _lib.mla_decode_mxfp4_ws(aq, akv, asc, dip.data_ptr(), dout.data_ptr(), B, float(sm_scale),
+                                          ms.cuda_stream, self._ws.data_ptr(), self._ws.numel())
+            if rc != _lib.MLA_OK:
+                raise _lib.MlaError(rc, "mla_decode_mxfp4_ws")
+            out_host.copy_(dout, non_blocking=True)
+        return out_host
+
     def __call__(self, q, kv_packed, kv_scale, kv_indptr, sm_scale, out_host: torch.Tensor) -> torch.Tensor:
+        if (self.direct and all(t.device.type == "cpu" and t.is_pinned() and t.is_contiguous()
+                                for t in (q, kv_packed, kv_scale, kv_indptr))):
+            return self._call_direct(q, kv_packed, kv_scale, kv_indptr, sm_scale, out_host)
         dq, dkv, dsc = self._buf("q", q), self._buf("kv", kv_packed), self._buf("sc", kv_scale)
         dip, dout = self._buf("ip", kv_indptr), self._buf("out", out_host)
         ip = kv_indptr.tolist()

@@ -535,6 +535,18 @@ void mla_decode_mxfp4_release(void) {
   if (prev >= 0) cudaSetDevice(prev);
 }
 
+int mla_host_device_pointer(const void* host, void** device) {
+  if (!host || !device) return MLA_ERR_NULL_PTR;
+  *device = nullptr;
+  // (an unregistered pointer is reported as such, not as an error, so the runtime's last-error
+  // state is left as it was)
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) return MLA_ERR_CUDA;
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return MLA_ERR_CUDA;
+  *device = a.devicePointer;
+  return MLA_OK;
+}
+
 const char* mla_status_string(int status) {
   switch (status) {
     case MLA_OK: return "MLA_OK";

@@ -25,6 +25,10 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_host_device_pointer_checks_its_arguments(L):
+    assert _lib.host_device_pointer(0) == (_lib.MLA_ERR_NULL_PTR, 0)
+
+
 def test_host_argument_checks(L):
     f = _lib.mla_decode_mxfp4
     ok = dict(q=0x1000, kv=0x2000, sc=0x3001, ip=0x4004, out=0x5000)  # kv_scale: no alignment rule

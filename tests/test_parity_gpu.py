@@ -409,13 +409,41 @@ def test_host_decoder_chunked_pipeline_matches_device_decode():
     hq, hkv, hsc, hip = (d.q.pin_memory(), d.kv_packed.pin_memory(), d.kv_scale.pin_memory(),
                          d.kv_indptr.pin_memory())
     for chunks in (1, 3, 8):
-        hd = HostDecoder(dev, chunks=chunks)
+        hd = HostDecoder(dev, chunks=chunks, direct=False)
         hout = torch.empty(d.batch, 16, 512, dtype=torch.bfloat16).pin_memory()
         for _ in range(2):  # the second call reuses the device buffers
             hout.fill_(float("nan"))
             hd(hq, hkv, hsc, hip, d.sm_scale, hout)
             hd.synchronize()
             check_close(as64(hout), ref, f"host decoder, {chunks} groups")
+
+
+def test_host_decoder_reading_pinned_inputs_in_place():
+    """The direct mode: the kernels read q, kv_packed and kv_scale straight from the pinned
+    host buffers (through mla_host_device_pointer); the output is bit-identical to the decode
+    of the same inputs copied to the device, and unpinned inputs fall back to the copies."""
+    from mla_decode_attention_mxfp4_gb300 import HostDecoder, _lib, decode
+    d = MI.make_custom([700, 0, 1500, 33, 2600, 1, 0, 900, 4100], seed=78)
+    dev = torch.device("cuda:0")
+    hq, hkv, hsc, hip = (d.q.pin_memory(), d.kv_packed.pin_memory(), d.kv_scale.pin_memory(),
+                         d.kv_indptr.pin_memory())
+    rc, addr = _lib.host_device_pointer(hkv.data_ptr())
+    assert rc == _lib.MLA_OK and addr != 0
+    rc, addr = _lib.host_device_pointer(d.kv_packed.data_ptr())  # pageable memory: refused
+    assert rc == _lib.MLA_ERR_CUDA and addr == 0
+    dev_out = decode(d.q.to(dev), d.kv_packed.to(dev), d.kv_scale.to(dev), d.kv_indptr.to(dev), d.sm_scale)
+    torch.cuda.synchronize()
+    hd = HostDecoder(dev, chunks=1)  # the copy path then decodes the batch in one call, as above
+    hout = torch.empty(d.batch, 16, 512, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        hout.fill_(float("nan"))
+        hd(hq, hkv, hsc, hip, d.sm_scale, hout)
+        hd.synchronize()
+        assert torch.equal(hout, dev_out.cpu())
+    hout.fill_(float("nan"))
+    hd(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale, hout)  # not pinned: copies
+    hd.synchronize()
+    assert torch.equal(hout, dev_out.cpu())
 
 
 def test_wait_limit_runs_out_cleanly_and_the_context_stays_usable():
