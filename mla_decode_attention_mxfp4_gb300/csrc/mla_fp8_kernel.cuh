@@ -2,11 +2,14 @@
 // "amd-mixed-mla" 676098 "_aiter_mla_decode" and 717900 "_decode": the pages' production path,
 // K[t][d] = kv[t][d] * kv_scale, V = K[:, :512]), for sm_103a.
 //
-// The tensor cores read e4m3 directly, so this kernel has no dequant group: per 128-token tile
+// The tensor cores read e4m3 directly, so this kernel has no dequant group: per 96-token tile
 // the producer warp brings the 576-byte rows into shared memory with five TMA tensor copies of
-// 128 rows x 128 bytes (the 128-byte swizzle; the last copy runs past the row and is zero-filled),
+// 96 rows x 128 bytes (the 128-byte swizzle; the last copy runs past the row and is zero-filled),
 // and the MMA warp runs QK^T with A = that tile (K-major) and P.V with A = the same tile read as
-// V^T (MN-major): the operand layouts of the two products coincide for these boxes.  The
+// V^T (MN-major): the operand layouts of the two products coincide for these boxes.  A tile
+// holds the stage 96 rows so that three stages fit beside the query operands; QK^T keeps
+// M = 128, and its rows 96..127 read the next box (finite data, their scores are masked)
+// while P.V sums over the 96 rows only.  The
 // partition, the query operand (two e4m3 terms per head) and the merge of split sequences are
 // those of the MXFP4 path; the softmax is the same online softmax with P' = 2^11 P as two e5m2
 // terms, the scores scaled by the per-head factor times kv_scale.  Rows of a tile past its
@@ -23,13 +26,14 @@
 namespace mla {
 namespace fp8 {
 
-constexpr int kTile = 128;
+constexpr int kTile = 96;    // tokens per tile: three stages fit beside the query operands
+constexpr int kMmaM = 128;   // M of the MMAs: QK^T rows 96..127 read the next box and are masked
 constexpr int kBoxBytes = 128;                        // inner extent of one copy = the swizzle span
 constexpr int kBoxes = (kDqk + kBoxBytes - 1) / kBoxBytes;  // 5: dims 0..639, 576.. zero-filled
 constexpr int kVBoxes = kDv / kBoxBytes;              // 4: the V part
-constexpr int kBoxTileBytes = kTile * kBoxBytes;      // 16384
-constexpr int kStageBytes = kBoxes * kBoxTileBytes;   // 81920
-constexpr int kStages = 2;
+constexpr int kBoxTileBytes = kTile * kBoxBytes;      // 12288
+constexpr int kStageBytes = kBoxes * kBoxTileBytes;   // 61440
+constexpr int kStages = 3;
 constexpr int kPrefetch = 2;  // lookahead of the L2 prefetch in tiles (see the producer)
 constexpr int kSmWarps = 4;
 constexpr int kSmThreads = kSmWarps * 32;
@@ -44,15 +48,15 @@ constexpr uint32_t kColO = 64;
 
 // Shared memory.
 constexpr int kOffStages = 0;                                      // boxes 1024-byte aligned
-constexpr int kOffQhat = kOffStages + kStages * kStageBytes;       // 163840: [2] query operands
-constexpr int kOffPt = kOffQhat + 2 * kQhatBytes;                  // 200704: [2] P^T
+constexpr int kOffQhat = kOffStages + kStages * kStageBytes;       // 184320: [2] query operands
+constexpr int kOffPt = kOffQhat + 2 * kQhatBytes;                  // 221184: [2] P^T
 constexpr int kOffHmax = kOffPt + 2 * kPtBytes;                    // [2][16 heads][4 quarters]
 constexpr int kOffLw = kOffHmax + 2 * 4 * kHeads * 4;              // [16 heads][4 quarters]
 constexpr int kOffMlast = kOffLw + 4 * kHeads * 4;                 // [16] output factors
 constexpr int kOffMst = kOffMlast + kHeads * 4;                    // [4 warps][16 m, 16 alpha]
 constexpr int kOffTmem = kOffMst + 4 * 2 * kHeads * 4;             // tensor-memory address, abort word
 constexpr int kOffBar = kOffTmem + 16;
-constexpr int kNumBars = 11;
+constexpr int kNumBars = 2 * kStages + 6;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8;
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffQhat % 1024 == 0 && kOffPt % 16 == 0, "operand alignment");
@@ -94,12 +98,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
   const int g = blockIdx.x;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* bar_full = bars;        // [2] stage landed (producer, tx bytes)
-  uint64_t* bar_empty = bars + 2;   // [2] stage read by QK^T and P.V (MMA commit)
-  uint64_t* bar_qfree = bars + 4;   // [2] query operand buffer read by its segment's last QK^T (MMA commit)
-  uint64_t* bar_qk = bars + 6;      // [2] S^T buffer written (MMA commit)
-  uint64_t* bar_pready = bars + 8;  // P^T written, invalid V rows zeroed, O^T rescaled (softmax group)
-  uint64_t* bar_pv = bars + 9;      // P.V of a tile completed (MMA commit)
+  uint64_t* bar_full = bars;                     // [kStages] stage landed (producer, tx bytes)
+  uint64_t* bar_empty = bars + kStages;          // [kStages] stage read by QK^T and P.V (MMA commit)
+  uint64_t* bar_qfree = bars + 2 * kStages;      // [2] query operand buffer read by its segment's last QK^T
+  uint64_t* bar_qk = bars + 2 * kStages + 2;     // [2] S^T buffer written (MMA commit)
+  uint64_t* bar_pready = bars + 2 * kStages + 4; // P^T written, invalid V rows zeroed, O^T rescaled (softmax)
+  uint64_t* bar_pv = bars + 2 * kStages + 5;     // P.V of a tile completed (MMA commit)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  TileIter it;
+  TileIterT<kTile> it;
   if (!it.init(p.ws.ipc, p.B, p.ws.cta_desc[2 * g], p.ws.cta_desc[2 * g + 1])) {
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
     return;
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
     // Two stages of 80 KB hold too few bytes in flight to cover the load latency, so when tile k
     // is copied, tile k + kPrefetch (which must wait for a stage) is prefetched into L2: its
     // copy, once a stage is free, then reads L2.
-    TileIter pf = it;
+    TileIterT<kTile> pf = it;
     bool pf_ok = true;
     for (int u = 0; u < kPrefetch && pf_ok; ++u) pf_ok = pf.next();
     int k = 0;
@@ -174,11 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
   // QK(0); then per tile k: QK(k+1) once its stage landed, P.V(k) once P^T(k) is ready; the
   // stage of tile k is released after P.V(k) (the commit covers QK(k), issued earlier).
   if (warp == kMmaWarp) {
-    const uint32_t idesc_qk = idesc_f8(kTile, 32, kFmtE4M3, kFmtE4M3, false, false);
-    const uint32_t idesc_pv = idesc_f8(kTile, 32, kFmtE4M3, kFmtE5M2, true, true);
+    const uint32_t idesc_qk = idesc_f8(kMmaM, 32, kFmtE4M3, kFmtE4M3, false, false);
+    const uint32_t idesc_pv = idesc_f8(kMmaM, 32, kFmtE4M3, kFmtE5M2, true, true);
     const uint64_t dq0 = smem_desc_kmajor(smem_u32(smem + kOffQhat), kQLbo, kQSbo);
     const uint64_t dp0 = smem_desc_mnmajor(smem_u32(smem + kOffPt), kPtLbo, kPtSbo);
-    TileIter cur = it, nxt = it;
+    TileIterT<kTile> cur = it, nxt = it;
     bool has_next = nxt.next();
     int k = 0;
     uint64_t* last_bar = nullptr;
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
       if (*abort_word_fp8()) break;
       if (kk == 0 || has_next) {
         const int q = kk;
-        const TileIter& qt = kk == 0 ? cur : nxt;
+        const TileIterT<kTile>& qt = kk == 0 ? cur : nxt;
         const int s = q % kStages;
         if (!wait_fp8(&bar_full[s], (q / kStages) & 1, p, aborted)) break;
         tc_fence_after();
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
       *reinterpret_cast<uint4*>(prow) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
       *reinterpret_cast<uint4*>(prow + kPtSbo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
     }
-    if (!valid) {  // this row of the stage holds another sequence's data: zero its V part
+    if (!valid && t < kTile) {  // this row of the stage holds another sequence's data: zero its V part
       uint8_t* vrow = smem + kOffStages + (k % kStages) * kStageBytes + t * kBoxBytes;
 #pragma unroll
       for (int x = 0; x < kVBoxes; ++x)

@@ -220,7 +220,8 @@ struct SplitParams {
 };
 
 // ---- tile iterator: identical walk for every role of a CTA --------------------
-struct TileIter {
+template <int kT>
+struct TileIterT {
   const int* ipc;
   int B;
   int b;       // sequence of the current segment
@@ -241,7 +242,7 @@ struct TileIter {
     b = d0.z;
     t0 = max(r0, d0.w);
     s1 = min(r1, d1.x);
-    n = min(kTile, s1 - t0);
+    n = min(kT, s1 - t0);
     seg = 0;
     first = true;
     last = t0 + n >= s1;
@@ -251,7 +252,7 @@ struct TileIter {
   __device__ bool next() {
     if (!last) {
       t0 += n;
-      n = min(kTile, s1 - t0);
+      n = min(kT, s1 - t0);
       first = false;
       last = t0 + n >= s1;
       return true;
@@ -263,13 +264,14 @@ struct TileIter {
     t0 = ipc[b];
     s1 = min(r1, ipc[b + 1]);
     whole = ipc[b + 1] <= r1;
-    n = min(kTile, s1 - t0);
+    n = min(kT, s1 - t0);
     ++seg;
     first = true;
     last = t0 + n >= s1;
     return true;
   }
 };
+using TileIter = TileIterT<kTile>;
 
 // ---- block-wide scans for the partition kernel (blockDim = 1024) -------------
 template <bool kMax>
