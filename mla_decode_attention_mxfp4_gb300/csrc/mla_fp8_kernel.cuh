@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
     if (lane != 0) return;
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    // Two stages of 80 KB hold too few bytes in flight to cover the load latency, so when tile k
-    // is copied, tile k + kPrefetch (which must wait for a stage) is prefetched into L2: its
+    // The stages (3 x 60 KB) hold too few bytes in flight to cover the load latency, so when tile
+    // k is copied, tile k + kPrefetch (which must wait for a stage) is prefetched into L2: its
     // copy, once a stage is free, then reads L2.
     TileIterT<kTile> pf = it;
     bool pf_ok = true;
