@@ -6,11 +6,10 @@
 // the producer warp brings the 576-byte rows into shared memory with five TMA tensor copies of
 // 96 rows x 128 bytes (the 128-byte swizzle; the last copy runs past the row and is zero-filled),
 // and the MMA warp runs QK^T with A = that tile (K-major) and P.V with A = the same tile read as
-// V^T (MN-major): the operand layouts of the two products coincide for these boxes.  A tile
-// holds the stage 96 rows so that three stages fit beside the query operands; QK^T keeps
-// M = 128, and its rows 96..127 read the next box (finite data, their scores are masked)
-// while P.V sums over the 96 rows only.  The
-// partition, the query operand (two e4m3 terms per head) and the merge of split sequences are
+// V^T (MN-major): the operand layouts of the two products coincide for these boxes.  Tiles of
+// 96 rows let three stages fit beside the query operands; QK^T keeps M = 128, and its rows
+// 96..127 read the next box (finite data, their scores are masked) while P.V sums over the 96
+// rows only.  The partition, the query operand (two e4m3 terms per head) and the merge of split sequences are
 // those of the MXFP4 path; the softmax is the same online softmax with P' = 2^11 P as two e5m2
 // terms, the scores scaled by the per-head factor times kv_scale.  Rows of a tile past its
 // sequence get -inf scores by selection, and their V rows are zeroed in shared memory before
