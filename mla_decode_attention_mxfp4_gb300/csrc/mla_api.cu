@@ -34,7 +34,7 @@ size_t g_ws_bytes[kMaxDevices] = {};
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsOffsets {
-  size_t meta, ipc, cta_desc, lse, acc, qhat, qch, kvc, qoc, phys, total;
+  size_t meta, ipc, cta_desc, lse, acc, qhat, qch, kvc, qoc, phys, tp, total;
 };
 
 WsOffsets ws_offsets(int batch, int grid) {
@@ -63,6 +63,8 @@ WsOffsets ws_offsets(int batch, int grid) {
   off = align_up(off + (size_t)(batch + 1) * sizeof(int), 256);
   o.phys = off;
   off = align_up(off + (size_t)batch * sizeof(int), 256);
+  o.tp = off;
+  off = align_up(off + (size_t)(batch + 1) * sizeof(int), 256);
   o.total = off;
   return o;
 }
@@ -80,6 +82,7 @@ mla::Workspace ws_bind(void* base, const WsOffsets& o) {
   w.kvc = reinterpret_cast<int*>(b + o.kvc);
   w.qoc = reinterpret_cast<int*>(b + o.qoc);
   w.phys = reinterpret_cast<int*>(b + o.phys);
+  w.tp = reinterpret_cast<int*>(b + o.tp);
   return w;
 }
 
@@ -108,8 +111,9 @@ int device_info(int dev, DeviceInfo* out) {
     if (prev != dev && prev >= 0) cudaSetDevice(prev);
     if (e != cudaSuccess || occ < 1 || occ8 < 1) return MLA_ERR_CUDA;
     d.sms = sms;
-    d.grid = sms * occ;
-    d.grid_fp8 = sms * occ8;
+    // the partition kernel cuts ranges for at most kPartMaxGrid CTAs
+    d.grid = sms * occ < mla::kPartMaxGrid ? sms * occ : mla::kPartMaxGrid;
+    d.grid_fp8 = sms * occ8 < mla::kPartMaxGrid ? sms * occ8 : mla::kPartMaxGrid;
     d.ws_grid = d.grid > d.grid_fp8 ? d.grid : d.grid_fp8;
     d.init = true;
   }
@@ -166,8 +170,9 @@ int launch(const void* q, const uint8_t* kv_packed, const uint8_t* kv_scale, con
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
+    const int tile = opt.fp8_map ? mla::fp8::kTile : mla::kTile;  // the split kernel's tile
     if (cudaLaunchKernelEx(&cfg, mla::mla_partition_kernel, kv_indptr, batch, grid, kv_null, w,
-                           static_cast<const __nv_bfloat16*>(q), sm_scale, opt.rm) != cudaSuccess)
+                           static_cast<const __nv_bfloat16*>(q), sm_scale, opt.rm, tile) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
   mla::SplitParams sp;
@@ -245,7 +250,8 @@ constexpr size_t kStaticScratchBytes =
     static_align(2 * (size_t)kStaticMaxGrid * mla::kHeads * mla::kDv * sizeof(float)) +
     static_align((size_t)kStaticMaxBatch * mla::kQhatBytes) +
     static_align((size_t)kStaticMaxBatch * mla::kHeads * sizeof(float)) +
-    2 * static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int)) + static_align((size_t)kStaticMaxBatch * sizeof(int));
+    2 * static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int)) + static_align((size_t)kStaticMaxBatch * sizeof(int)) +
+    static_align((size_t)(kStaticMaxBatch + 1) * sizeof(int));
 
 // One copy per GPU that loads the library, alive until the process exits.
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];

@@ -9,10 +9,11 @@
 // mla_reduce_v1_like_kernel / 676098 _mla_reduce_kernel), but the partition is
 // built on the device and the per-split arithmetic is organised for GB300:
 //
-//  1. mla_partition_kernel: its first CTA sanitises kv_indptr, cuts the concatenated
-//     token stream [indptr[0], indptr[B]) into G equal contiguous ranges (one per
-//     resident CTA), and writes one work descriptor per range (partial slots are
-//     fixed by range, so the merge derives them from kv_indptr); the other CTAs
+//  1. mla_partition_kernel: its first CTA sanitises kv_indptr, counts each sequence's
+//     tiles, cuts the concatenated token stream [indptr[0], indptr[B]) into G contiguous
+//     ranges of whole tiles (one per resident CTA, at most one tile apart in size), and
+//     writes one work descriptor per range (partial slots are fixed by range, so the
+//     merge derives them from the tile counts); the other CTAs
 //     build each sequence's query operand
 //     (e4m3 hi/lo parts of the prescaled query, in its shared-memory image) and
 //     the per-head score factors.
@@ -91,14 +92,14 @@ constexpr int kSmWarp0 = 2;                  // softmax group: warps 2..5
 constexpr int kDqWarp0 = kSmWarp0 + kSmWarps;  // dequant group: warps 6..17
 constexpr int kRefWarp = kDqWarp0 + kDqWarps;   // tile reference exponents: warp 18
 constexpr int kThreads = (kTokWarps + 3) * 32;
-constexpr int kMinPerCta = 64; // smallest token range given to one CTA
 constexpr int kPartSmemSeqs = 8192;  // the partition kernel keeps ipc in shared memory up to this batch
+constexpr int kPartMaxGrid = 1024;   // most split CTAs the partition kernel cuts ranges for
 
 constexpr int kDeviceBadIndptr = 1;
 constexpr int kDeviceTimeout = 2;
 
 // meta[] fields written by the partition kernel
-enum MetaField { kMetaN = 0, kMetaPer = 1, kMetaGeff = 2, kMetaStatus = 3, kMetaRows = 4 };
+enum MetaField { kMetaN = 0, kMetaTiles = 1, kMetaGeff = 2, kMetaStatus = 3, kMetaRows = 4 };
 
 // Partial slots: range g's first segment writes slot 2g and its last segment slot 2g + 1
 // when they are parts of split sequences (any other segment of a range is a whole
@@ -120,6 +121,7 @@ struct Workspace {
   int* kvc;           // [Bkv+1] sanitised kv_indptr (general layout only)
   int* qoc;           // [Bkv+1] sanitised qo_indptr for more than kPartSmemSeqs sequences (general layout)
   int* phys;          // [S] first physical row, or first entry of kv_indices (general layout only)
+  int* tp;            // [S+1] tiles of the split kernel in the sequences before each one
 };
 
 // Layout of the KV rows beyond the plain one (kv_indptr rows, one query row per sequence).
@@ -382,7 +384,7 @@ constexpr int kQhatSeqsPerBlock = kPartThreads / 32 / kHeads;  // 2
 __global__ void __launch_bounds__(kPartThreads, 1) mla_partition_kernel(const int32_t* __restrict__ indptr, int B,
                                                                      int G, int kv_null, Workspace ws,
                                                                      const __nv_bfloat16* __restrict__ q,
-                                                                     float sm_scale, RowMap rm) {
+                                                                     float sm_scale, RowMap rm, int tile) {
   grid_launch_dependents();  // the split kernel's prologue may run alongside
   // Launched with programmatic serialization, this grid may be resident before the
   // preceding kernel in the stream (the previous call's merge kernel, or whatever wrote
@@ -397,6 +399,8 @@ __global__ void __launch_bounds__(kPartThreads, 1) mla_partition_kernel(const in
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_ipc[kPartSmemSeqs + 1];  // copy of ipc for batch <= kPartSmemSeqs
+  __shared__ int s_cut[kPartMaxGrid + 1];   // first row of each range, and the end
+  __shared__ int s_first[kPartMaxGrid];     // first sequence of each range
   const bool in_smem = B <= kPartSmemSeqs;
   const bool general = rm.qo_indptr != nullptr || rm.kv_indices != nullptr;
   if (tid == 0) s_bad = 0;
@@ -530,22 +534,43 @@ __global__ void __launch_bounds__(kPartThreads, 1) mla_partition_kernel(const in
   const int* ipc = in_smem ? s_ipc : ws.ipc;
   const int rbase = ipc[0];
   const int N = ipc[B] - rbase;
-  const long long per_ll = max((long long)kMinPerCta, ((long long)N + G - 1) / G);
-  const int per = (int)per_ll;
-  const int geff = N > 0 ? (int)(((long long)N + per - 1) / per) : 0;
-  // per range: its rows, its first sequence (largest b with ipc[b] <= r0) and that
-  // sequence's rows, so a CTA starts from one 32-byte load; empty ranges have r0 == r1
+  // Tiles: each sequence is walked in tiles of `tile` rows from its first row, the last one
+  // possibly short; tp[b] counts the tiles of the sequences before b.  A tile costs the split
+  // kernel the same time however many of its rows are used, so the ranges are cut in whole
+  // tiles: range g gets tiles [x_g, x_{g+1}), x_g = floor(g T / geff), geff = min(G, T).
+  int T = 0;
+  for (int base = 0; base <= B; base += 1024) {
+    const int i = base + tid;
+    const int nt = i < B ? (ipc[i + 1] - ipc[i] + tile - 1) / tile : 0;
+    int tot;
+    const int incl = block_inclusive_scan<false>(nt, warp_tot, tot);
+    if (i <= B) ws.tp[i] = T + incl - nt;
+    T += tot;
+  }
+  const int geff = min(G, T);
+  __threadfence_block();
+  __syncthreads();
+  // the first row of each range and its first sequence: range g starts in the sequence whose
+  // tiles hold x_g, at row ipc[b] + (x_g - tp[b]) tile
+  for (int b = tid; b < B; b += 1024) {
+    const int t0 = ws.tp[b], t1 = ws.tp[b + 1];
+    if (t1 <= t0) continue;
+    const int g0 = (int)(((long long)t0 * geff + T - 1) / T), g1 = (int)(((long long)t1 * geff + T - 1) / T);
+    for (int g = g0; g < g1; ++g) {
+      const int x = (int)((long long)g * T / geff);
+      s_cut[g] = ipc[b] + (x - t0) * tile;
+      s_first[g] = b;
+    }
+  }
+  if (tid == 0) s_cut[geff] = rbase + N;
+  __syncthreads();
+  // per range: its rows, its first sequence and that sequence's rows, so a CTA starts from
+  // one 32-byte load; empty ranges have r0 == r1
   for (int g = tid; g < G; g += 1024) {
     int4 d0 = make_int4(0, 0, 0, 0), d1 = make_int4(0, 0, 0, 0);
     if (g < geff) {
-      const int r0 = rbase + g * per;
-      int lo = 0, hi2 = B - 1;
-      while (lo < hi2) {
-        const int mid = (lo + hi2 + 1) >> 1;
-        if (ipc[mid] <= r0) lo = mid;
-        else hi2 = mid - 1;
-      }
-      d0 = make_int4(r0, (int)min((long long)ipc[B], (long long)r0 + per), lo, ipc[lo]);
+      const int lo = s_first[g];
+      d0 = make_int4(s_cut[g], s_cut[g + 1], lo, ipc[lo]);
       d1.x = ipc[lo + 1];
     }
     ws.cta_desc[2 * g] = d0;
@@ -553,7 +578,7 @@ __global__ void __launch_bounds__(kPartThreads, 1) mla_partition_kernel(const in
   }
   if (tid == 0) {
     ws.meta[kMetaN] = N;
-    ws.meta[kMetaPer] = per;
+    ws.meta[kMetaTiles] = T;
     ws.meta[kMetaGeff] = geff;
     ws.meta[kMetaStatus] = s_bad ? kDeviceBadIndptr : 0;
   }
@@ -1319,15 +1344,20 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16*
   // after griddepcontrol.wait.
   const int b = blockIdx.x;
   const int tid = threadIdx.x, h = (tid >> 5) + kMergeHeads * blockIdx.y, lane = tid & 31;
-  const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1], rbase = ws.ipc[0], per = ws.meta[kMetaPer];
+  const int a0 = ws.ipc[b], a1 = ws.ipc[b + 1];
   uint4* dst = reinterpret_cast<uint4*>(out + ((long long)b * kHeads + h) * kDv + lane * 16);
-  int f = 0, ns = 0;
+  int f = 0, ns = 0, shift0 = 0;
   if (a1 <= a0) {  // empty sequence -> zeros (the split kernel writes no row of it)
     dst[0] = make_uint4(0, 0, 0, 0);
     dst[1] = make_uint4(0, 0, 0, 0);
   } else {
-    f = (a0 - rbase) / per;
-    ns = (a1 - 1 - rbase) / per - f + 1;  // ns == 1: a whole sequence, written by the split kernel
+    // ranges f .. f + ns - 1 hold the sequence's tiles tp[b] .. tp[b+1] - 1 (range g holds tiles
+    // from floor(g T / geff)); ns == 1: a whole sequence, written by the split kernel
+    const long long T = ws.meta[kMetaTiles], geff = ws.meta[kMetaGeff];
+    const int t0 = ws.tp[b], t1 = ws.tp[b + 1];
+    f = (int)(((t0 + 1) * geff - 1) / T);
+    ns = (int)((t1 * geff - 1) / T) - f + 1;
+    shift0 = (int)(f * T / geff) != t0 ? 1 : 0;
   }
   // Every CTA waits for the split grid, also those with nothing to merge: this grid must not
   // complete before its predecessor, since the next kernel in the stream (launched
@@ -1337,7 +1367,6 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(__nv_bfloat16*
   if (ns < 2) return;
   // partial i of this sequence is in slot 2(f + i), the first one shifted by one when the
   // sequence is not the first of range f
-  const int shift0 = a0 != rbase + f * per ? 1 : 0;
   auto slot_of = [&](int i) { return 2 * (f + i) + (i == 0 ? shift0 : 0); };
   // the rows of up to kPre partials are requested together with the weights (one round
   // trip to memory for splits of up to kPre ways)

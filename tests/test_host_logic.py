@@ -6,17 +6,20 @@ token row is visited exactly once, all reads stay inside [0, kv_indptr[batch])
 rows and inside the caller's scale bytes, every smem copy fits its stage, and
 partial slots (range g's first segment -> slot 2g, its last -> 2g + 1) are
 unique, below the workspace bound of 2 slots per CTA, and exactly the slots
-the merge kernel derives for each split sequence from kv_indptr alone.
+the merge kernel derives for each split sequence from the tile prefix alone.
 """
 import random
 
 import pytest
 
-TILE, PACKED, NSCALE, MIN_PER = 128, 288, 18, 64
+TILE, PACKED, NSCALE = 128, 288, 18
+FP8_TILE = 96
 STAGE_SCALE_BYTES = 2432
 
 
-def partition(indptr, G, kv_null=False):
+def partition(indptr, G, kv_null=False, tile=TILE):
+    """ipc (sanitised kv_indptr), tp (tiles before each sequence), T, geff, the ranges' first
+    rows (and the end) and their first sequences, and the malformed-input flag."""
     B = len(indptr) - 1
     hi = 0 if kv_null else max(indptr[B], 0)
     ipc, pm, bad = [], None, False
@@ -25,40 +28,41 @@ def partition(indptr, G, kv_null=False):
             bad = True
         pm = v if pm is None else max(pm, v)
         ipc.append(min(max(pm, 0), hi))
-    N = ipc[B] - ipc[0]
-    per = max(MIN_PER, -(-N // G))
-    geff = -(-N // per) if N > 0 else 0
-    cta_first = []
+    tp = [0]
+    for b in range(B):
+        tp.append(tp[-1] + -(-(ipc[b + 1] - ipc[b]) // tile))
+    T = tp[B]
+    geff = min(G, T)
+    cuts, firsts = [], []
     for g in range(geff):
-        r0 = ipc[0] + g * per
-        cta_first.append(max(b for b in range(B) if ipc[b] <= r0))
-    return ipc, per, geff, cta_first, bad
+        x = g * T // geff  # range g holds tiles [x_g, x_{g+1})
+        b = next(b for b in range(B) if tp[b] <= x < tp[b + 1])
+        cuts.append(ipc[b] + (x - tp[b]) * tile)
+        firsts.append(b)
+    cuts.append(ipc[B])
+    return ipc, tp, T, geff, cuts, firsts, bad
 
 
-def merge_slots(ipc, per, b):
+def merge_slots(ipc, tp, T, geff, b):
     """Slots the merge kernel reads for sequence b (None: whole or empty sequence)."""
-    a0, a1, rbase = ipc[b], ipc[b + 1], ipc[0]
-    if a1 <= a0:
+    if ipc[b + 1] <= ipc[b]:
         return None
-    f, l = (a0 - rbase) // per, (a1 - 1 - rbase) // per
+    t0, t1 = tp[b], tp[b + 1]
+    f, l = ((t0 + 1) * geff - 1) // T, (t1 * geff - 1) // T
     if f == l:
         return None
-    shift0 = 1 if a0 != rbase + f * per else 0
+    shift0 = 1 if f * T // geff != t0 else 0
     return [2 * (f + i) + (shift0 if i == 0 else 0) for i in range(l - f + 1)]
 
 
-def tiles(ipc, B, g, per, first_seq):
-    rend = ipc[B]
-    r0 = ipc[0] + g * per
-    if r0 >= rend:
-        return []
-    r1 = min(rend, r0 + per)
+def tiles(ipc, B, r0, r1, first_seq, tile=TILE):
+    """The split kernel's tile walk of range [r0, r1) (TileIterT)."""
     b = first_seq
     t0 = max(r0, ipc[b])
     s1 = min(r1, ipc[b + 1])
     out, seg, first = [], 0, True
     while True:
-        n = min(TILE, s1 - t0)
+        n = min(tile, s1 - t0)
         assert n > 0
         out.append((b, seg, t0, n, first, t0 + n >= s1))
         if t0 + n < s1:
@@ -87,9 +91,9 @@ def scale_copy_plan(t0, n, mis, scale_end):
     return b0, b1, a0, plain, bulk
 
 
-def check(indptr, G=152, kv_null=False, mis=0):
+def check(indptr, G=152, kv_null=False, mis=0, tile=TILE):
     B = len(indptr) - 1
-    ipc, per, geff, cta_first, bad = partition(indptr, G, kv_null)
+    ipc, tp, T, geff, cuts, firsts, bad = partition(indptr, G, kv_null, tile)
     rows_limit = 0 if kv_null else max(indptr[B], 0)  # caller guarantees indptr[batch] rows
     assert all(ipc[i] <= ipc[i + 1] for i in range(B))
     assert geff <= G
@@ -98,13 +102,16 @@ def check(indptr, G=152, kv_null=False, mis=0):
     slots_of = {}
     scale_end = mis + ipc[B] * NSCALE  # the buffer is [mis, mis + 18 * rows) from the boundary below it
     for g in range(geff):
-        tl = tiles(ipc, B, g, per, cta_first[g])
-        assert tl, g
+        tl = tiles(ipc, B, cuts[g], cuts[g + 1], firsts[g], tile)
+        # ranges are cut in whole tiles: range g walks exactly its tiles, and none holds more
+        # than ceil(T / geff) of them
+        assert len(tl) == (g + 1) * T // geff - g * T // geff, g
+        assert len(tl) <= -(-T // geff)
         for (b, seg, t0, n, first, last) in tl:
             if first:
                 seg_start = t0
             assert 0 <= ipc[b] <= t0 and t0 + n <= ipc[b + 1] <= rows_limit
-            assert 1 <= n <= TILE
+            assert 1 <= n <= tile
             for r in range(t0, t0 + n):
                 assert r not in seen
                 seen.add(r)
@@ -130,7 +137,7 @@ def check(indptr, G=152, kv_null=False, mis=0):
                     slots_of.setdefault(b, []).append(slot)
     assert sorted(seen) == list(range(ipc[0], ipc[B]))
     for b in range(B):
-        assert merge_slots(ipc, per, b) == slots_of.get(b), b
+        assert merge_slots(ipc, tp, T, geff, b) == slots_of.get(b), b
     return bad
 
 
@@ -150,7 +157,7 @@ def test_partition_covers_every_row_once(G):
             ip.append(ip[-1] + x)
         cases.append(ip)
     for i, ip in enumerate(cases):
-        assert not check(ip, G, mis=(0, 1, 7, 15)[i % 4])
+        assert not check(ip, G, mis=(0, 1, 7, 15)[i % 4], tile=(TILE, FP8_TILE)[i % 2])
 
 
 def test_ragged_workload_partition():
@@ -161,6 +168,16 @@ def test_ragged_workload_partition():
     for x in lens:
         ip.append(ip[-1] + x)
     assert not check(ip, 152)
+    assert not check(ip, 152, tile=FP8_TILE)
+
+
+def test_uniform_ranges_hold_whole_tiles():
+    # 128 sequences of 4096 rows: 4096 tiles over 152 ranges, none cut inside a tile
+    ip = [4096 * i for i in range(129)]
+    ipc, tp, T, geff, cuts, firsts, bad = partition(ip, 152)
+    assert T == 4096 and geff == 152
+    assert all((c - ipc[b]) % TILE == 0 for c, b in zip(cuts, firsts))
+    assert max((g + 1) * T // geff - g * T // geff for g in range(geff)) == 27
 
 
 def test_malformed_indptr_is_clamped_and_flagged():
