@@ -575,6 +575,28 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+def run_profile_workload(args):
+    """A fixed number of launches of one workload and nothing else (no soak, no end-to-end leg),
+    so that a profiler can address one launch by its index: --warmup calls, then --steps timed
+    calls.  Prints one short JSON line."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import mla_inputs as MI
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    name = args.profile_workload
+    W = GeneralWorkload(name, dev, stream) if ":" in name else DeviceWorkload(MI.make_inputs(name), dev, stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            W.call(i)
+        ms = W.time_calls(args.steps)
+    print(json.dumps({"profile_workload": name, "launches_of_the_split_kernel": args.warmup + args.steps,
+                      "us_per_call": ms * 1e3}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -586,11 +608,15 @@ def main():
     ap.add_argument("--extra", nargs="*",
                     default=["ragged", "uniform:fp8", "ragged:fp8", "ragged:paged64", "uniform:q2"],
                     help="further workloads measured on the device and reported under extra_workloads")
+    ap.add_argument("--profile-workload", default=None,
+                    help="only --warmup + --steps calls of this workload (e.g. ragged:paged64), for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile_workload:
+        run_profile_workload(args)
     else:
         run_native(args)
 
