@@ -769,7 +769,140 @@ __device__ __noinline__ void reference_warp(uint8_t* smem, uint64_t* bar_full, u
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParams p) {
+// Producer warp of mla_split_kernel, one thread (out of line, like the reference warp: its
+// code lies apart from the other roles').  It walks the tiles in the CTA's order and fills
+// stage k % kStages once the dequant group released it: packed rows and scale bytes by bulk
+// copies, and the sequence's query operand into buffer (segment & 1) at a segment start.
+__device__ __noinline__ void producer_warp(uint8_t* smem, const SplitParams& pp, TileIter it, uint64_t* bar_full,
+                                           uint64_t* bar_empty, uint64_t* bar_qfree) {
+  const SplitParams p = pp;  // the fields in registers
+  bool aborted = false;
+  const uint64_t pol_kv = policy_evict_first();
+  const uint64_t pol_q = policy_evict_last();
+  // scale byte x of physical row r is at sc[sc_mis + 18r]; the bytes in use end at scale_end, and
+  // the buffer's first 16-byte boundary is head16
+  const long long scale_end = p.sc_mis + (long long)p.ws.meta[kMetaRows] * kNScale;
+  const long long scale_end16 = scale_end & ~15LL;
+  const long long head16 = (p.sc_mis + 15) & ~15LL;
+  // Paged layout: the run of the tile's tokens that starts at tile row i lies in one page:
+  // `cnt` rows from physical row `row`.
+  // Paged layout: the sequence's logical start and its first kv_indices entry are loaded
+  // once per segment; a tile's page ids (at most kTilePidSlots of them when page_size >= 9)
+  // are loaded together and kept in shared memory while one pass walks the runs.
+  int* pid_s = reinterpret_cast<int*>(smem + kOffPid);
+  int seg_b = -1, seg_pos0 = 0, seg_ix0 = 0;
+  int k = 0;
+  if (!p.stall_producer) do {
+    const int s = k % kStages;
+    if (k >= kStages && !wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted)) break;
+    const int j = it.seg;
+    // segment j's Qhat goes to buffer j & 1 once the last QK^T of segment j - 2 read it
+    if (it.first && j >= 2 && !wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted))
+      break;
+    uint8_t* st = smem + kOffStages + s * kStageBytes;
+    uint8_t* sdst = st + kStagePackedBytes;
+    if (p.rmode != kRowModePaged) {
+      // one run of rows from physical row row0 (row0 = t0 in the plain layout)
+      const long long row0 =
+          it.t0 + (p.rmode == kRowModeContig ? (long long)p.ws.phys[it.b] - p.ws.ipc[it.b] : 0LL);
+      // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
+      // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
+      // buffer's first boundary and past its last one by plain loads
+      const long long b0 = p.sc_mis + row0 * kNScale, b1 = b0 + (long long)it.n * kNScale;
+      const long long a0 = b0 & ~15LL;
+      const long long c0 = a0 > head16 ? a0 : head16;
+      long long a1 = (b1 + 15) & ~15LL;
+      if (a1 > scale_end16) a1 = scale_end16;
+      for (long long x = b0; x < b1 && x < c0; ++x) sdst[x - a0] = p.sc[x];
+      for (long long x = (a1 > c0 ? a1 : c0); x < b1; ++x) sdst[x - a0] = p.sc[x];
+      *reinterpret_cast<int*>(st + kStageMisOff) = (int)(b0 & 15);
+      uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > c0 ? (uint32_t)(a1 - c0) : 0u);
+      if (it.first) bytes += kQhatBytes;
+      mbar_arrive_expect_tx(&bar_full[s], bytes);
+      bulk_g2s(st, p.kv + row0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
+      if (a1 > c0) bulk_g2s(sdst + (c0 - a0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+    } else {
+      // Paged: one run per page the tile touches.  A run's scale bytes [g0, g1) land at stage
+      // offset dst0 + (x - g0), dst0 = M + 18 i: the 16-byte chunks [c0, a1) by bulk copy when
+      // source and destination agree modulo 16, the other bytes by plain loads.  At the tile's
+      // own ends the bulk range may round outwards (the extra bytes land outside the tile's
+      // part of the area); between runs it rounds inwards.  One pass over the runs issues the
+      // plain loads and the bulk copies and counts the bulk bytes; the stage is announced with
+      // that count afterwards (the barrier's transaction count may run below zero until then,
+      // and the phase cannot complete before this thread's arrival).
+      if (it.b != seg_b) {
+        seg_b = it.b;
+        seg_pos0 = p.ws.ipc[seg_b];
+        seg_ix0 = p.ws.phys[seg_b];
+      }
+      const int ps = p.page_size;
+      const int pos0 = it.t0 - seg_pos0;
+      const int pg0 = pos0 / ps, off0 = pos0 - pg0 * ps;
+      const int npg = (off0 + it.n + ps - 1) / ps;  // pages the tile touches
+      const bool in_smem = npg <= kTilePidSlots;
+      auto clamp_page = [&](int page) {  // an id outside the buffers is clamped into them, and flagged
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
+          page = min(max(page, 0), max(p.num_pages - 1, 0));
+        }
+        return page;
+      };
+      if (in_smem) {
+        const int* src = p.kv_indices + seg_ix0 + pg0;
+        int u = 0;
+        for (; u + 4 <= npg; u += 4) {  // four loads in flight, then their stores
+          const int a0 = src[u], a1v = src[u + 1], a2 = src[u + 2], a3 = src[u + 3];
+          pid_s[u] = clamp_page(a0);
+          pid_s[u + 1] = clamp_page(a1v);
+          pid_s[u + 2] = clamp_page(a2);
+          pid_s[u + 3] = clamp_page(a3);
+        }
+        for (; u < npg; ++u) pid_s[u] = clamp_page(src[u]);
+      }
+      int M = 0;
+      uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
+      for (int u = 0; u < npg; ++u) {
+        // run u: tile rows [i, i + cnt) from physical row `row`
+        const int page = in_smem ? pid_s[u] : clamp_page(p.kv_indices[seg_ix0 + pg0 + u]);
+        const int off = u == 0 ? off0 : 0;
+        const int i = u == 0 ? 0 : ps * u - off0;
+        const int cnt = min(ps - off, it.n - i);
+        const long long row = (long long)page * ps + off;
+        const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
+        if (u == 0) M = (int)(g0 & 15);
+        const long long dst0 = M + (long long)i * kNScale;
+        long long c0 = g1, a1 = g1;  // no bulk range
+        if (((g0 - dst0) & 15) == 0) {
+          c0 = i == 0 ? (g0 & ~15LL) : ((g0 + 15) & ~15LL);
+          a1 = i + cnt == it.n ? ((g1 + 15) & ~15LL) : (g1 & ~15LL);
+          if (c0 < head16) c0 = head16;
+          if (a1 > scale_end16) a1 = scale_end16;
+          if (a1 < c0) a1 = c0;
+        }
+        for (long long x = g0; x < g1 && x < c0; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+        for (long long x = (a1 > g0 ? a1 : g0); x < g1; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
+        bytes += (uint32_t)cnt * kPacked + (uint32_t)(a1 - c0);
+        bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
+        if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
+      }
+      *reinterpret_cast<int*>(st + kStageMisOff) = M;
+      mbar_arrive_expect_tx(&bar_full[s], bytes);
+    }
+    if (it.first)
+      bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
+               &bar_full[s], pol_q);
+    ++k;
+  } while (!*abort_word() && it.next());
+  // Drain before this warp leaves: the last phase issued on each stage completes once its
+  // copies have landed (in a normal run the dequant group has waited for all of them; after
+  // an abort it may not have, and no copy may still be writing when the CTA exits).
+  for (int s = 0; s < kStages && s < k; ++s) {
+    const int kl = s + ((k - 1 - s) / kStages) * kStages;  // last tile issued on stage s
+    mbar_wait(&bar_full[s], (uint32_t)(kl / kStages) & 1u, p.timeout_ns);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const __grid_constant__ SplitParams p) {
   uint8_t* smem = dyn_smem;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -825,129 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const SplitParam
   // =========================== producer warp ===================================
   if (warp == kProdWarp) {
     if (lane != 0) return;
-    const uint64_t pol_kv = policy_evict_first();
-    const uint64_t pol_q = policy_evict_last();
-    // scale byte x of physical row r is at sc[sc_mis + 18r]; the bytes in use end at scale_end, and
-    // the buffer's first 16-byte boundary is head16
-    const long long scale_end = p.sc_mis + (long long)p.ws.meta[kMetaRows] * kNScale;
-    const long long scale_end16 = scale_end & ~15LL;
-    const long long head16 = (p.sc_mis + 15) & ~15LL;
-    // Paged layout: the run of the tile's tokens that starts at tile row i lies in one page:
-    // `cnt` rows from physical row `row`.
-    // Paged layout: the sequence's logical start and its first kv_indices entry are loaded
-    // once per segment; a tile's page ids (at most kTilePidSlots of them when page_size >= 9)
-    // are loaded together and kept in shared memory while one pass walks the runs.
-    int* pid_s = reinterpret_cast<int*>(smem + kOffPid);
-    int seg_b = -1, seg_pos0 = 0, seg_ix0 = 0;
-    int k = 0;
-    if (!p.stall_producer) do {
-      const int s = k % kStages;
-      if (k >= kStages && !wait_or_flag(&bar_empty[s], ((k / kStages) - 1) & 1, p, aborted)) break;
-      const int j = it.seg;
-      // segment j's Qhat goes to buffer j & 1 once the last QK^T of segment j - 2 read it
-      if (it.first && j >= 2 && !wait_or_flag(&bar_qfree[j & 1], ((j >> 1) - 1) & 1, p, aborted))
-        break;
-      uint8_t* st = smem + kOffStages + s * kStageBytes;
-      uint8_t* sdst = st + kStagePackedBytes;
-      if (p.rmode != kRowModePaged) {
-        // one run of rows from physical row row0 (row0 = t0 in the plain layout)
-        const long long row0 =
-            it.t0 + (p.rmode == kRowModeContig ? (long long)p.ws.phys[it.b] - p.ws.ipc[it.b] : 0LL);
-        // the tile's scale bytes [b0, b1) land at stage offset x - a0 (a0 = b0 rounded down to 16):
-        // the 16-byte chunks inside the buffer [c0, a1) by bulk copy, the bytes before the
-        // buffer's first boundary and past its last one by plain loads
-        const long long b0 = p.sc_mis + row0 * kNScale, b1 = b0 + (long long)it.n * kNScale;
-        const long long a0 = b0 & ~15LL;
-        const long long c0 = a0 > head16 ? a0 : head16;
-        long long a1 = (b1 + 15) & ~15LL;
-        if (a1 > scale_end16) a1 = scale_end16;
-        for (long long x = b0; x < b1 && x < c0; ++x) sdst[x - a0] = p.sc[x];
-        for (long long x = (a1 > c0 ? a1 : c0); x < b1; ++x) sdst[x - a0] = p.sc[x];
-        *reinterpret_cast<int*>(st + kStageMisOff) = (int)(b0 & 15);
-        uint32_t bytes = (uint32_t)it.n * kPacked + (a1 > c0 ? (uint32_t)(a1 - c0) : 0u);
-        if (it.first) bytes += kQhatBytes;
-        mbar_arrive_expect_tx(&bar_full[s], bytes);
-        bulk_g2s(st, p.kv + row0 * kPacked, (uint32_t)it.n * kPacked, &bar_full[s], pol_kv);
-        if (a1 > c0) bulk_g2s(sdst + (c0 - a0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
-      } else {
-        // Paged: one run per page the tile touches.  A run's scale bytes [g0, g1) land at stage
-        // offset dst0 + (x - g0), dst0 = M + 18 i: the 16-byte chunks [c0, a1) by bulk copy when
-        // source and destination agree modulo 16, the other bytes by plain loads.  At the tile's
-        // own ends the bulk range may round outwards (the extra bytes land outside the tile's
-        // part of the area); between runs it rounds inwards.  One pass over the runs issues the
-        // plain loads and the bulk copies and counts the bulk bytes; the stage is announced with
-        // that count afterwards (the barrier's transaction count may run below zero until then,
-        // and the phase cannot complete before this thread's arrival).
-        if (it.b != seg_b) {
-          seg_b = it.b;
-          seg_pos0 = p.ws.ipc[seg_b];
-          seg_ix0 = p.ws.phys[seg_b];
-        }
-        const int ps = p.page_size;
-        const int pos0 = it.t0 - seg_pos0;
-        const int pg0 = pos0 / ps, off0 = pos0 - pg0 * ps;
-        const int npg = (off0 + it.n + ps - 1) / ps;  // pages the tile touches
-        const bool in_smem = npg <= kTilePidSlots;
-        auto clamp_page = [&](int page) {  // an id outside the buffers is clamped into them, and flagged
-          if (page < 0 || page >= p.num_pages) {
-            atomicOr(&p.ws.meta[kMetaStatus], kDeviceBadIndptr);
-            page = min(max(page, 0), max(p.num_pages - 1, 0));
-          }
-          return page;
-        };
-        if (in_smem) {
-          const int* src = p.kv_indices + seg_ix0 + pg0;
-          int u = 0;
-          for (; u + 4 <= npg; u += 4) {  // four loads in flight, then their stores
-            const int a0 = src[u], a1v = src[u + 1], a2 = src[u + 2], a3 = src[u + 3];
-            pid_s[u] = clamp_page(a0);
-            pid_s[u + 1] = clamp_page(a1v);
-            pid_s[u + 2] = clamp_page(a2);
-            pid_s[u + 3] = clamp_page(a3);
-          }
-          for (; u < npg; ++u) pid_s[u] = clamp_page(src[u]);
-        }
-        int M = 0;
-        uint32_t bytes = it.first ? (uint32_t)kQhatBytes : 0u;
-        for (int u = 0; u < npg; ++u) {
-          // run u: tile rows [i, i + cnt) from physical row `row`
-          const int page = in_smem ? pid_s[u] : clamp_page(p.kv_indices[seg_ix0 + pg0 + u]);
-          const int off = u == 0 ? off0 : 0;
-          const int i = u == 0 ? 0 : ps * u - off0;
-          const int cnt = min(ps - off, it.n - i);
-          const long long row = (long long)page * ps + off;
-          const long long g0 = p.sc_mis + row * kNScale, g1 = g0 + (long long)cnt * kNScale;
-          if (u == 0) M = (int)(g0 & 15);
-          const long long dst0 = M + (long long)i * kNScale;
-          long long c0 = g1, a1 = g1;  // no bulk range
-          if (((g0 - dst0) & 15) == 0) {
-            c0 = i == 0 ? (g0 & ~15LL) : ((g0 + 15) & ~15LL);
-            a1 = i + cnt == it.n ? ((g1 + 15) & ~15LL) : (g1 & ~15LL);
-            if (c0 < head16) c0 = head16;
-            if (a1 > scale_end16) a1 = scale_end16;
-            if (a1 < c0) a1 = c0;
-          }
-          for (long long x = g0; x < g1 && x < c0; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
-          for (long long x = (a1 > g0 ? a1 : g0); x < g1; ++x) sdst[dst0 + (x - g0)] = p.sc[x];
-          bytes += (uint32_t)cnt * kPacked + (uint32_t)(a1 - c0);
-          bulk_g2s(st + i * kPacked, p.kv + row * kPacked, (uint32_t)cnt * kPacked, &bar_full[s], pol_kv);
-          if (a1 > c0) bulk_g2s(sdst + dst0 + (c0 - g0), p.sc + c0, (uint32_t)(a1 - c0), &bar_full[s], pol_kv);
-        }
-        *reinterpret_cast<int*>(st + kStageMisOff) = M;
-        mbar_arrive_expect_tx(&bar_full[s], bytes);
-      }
-      if (it.first)
-        bulk_g2s(smem + kOffQhat + (j & 1) * kQhatBytes, p.ws.qhat + (long long)it.b * kQhatBytes, kQhatBytes,
-                 &bar_full[s], pol_q);
-      ++k;
-    } while (!*abort_word() && it.next());
-    // Drain before this warp leaves: the last phase issued on each stage completes once its
-    // copies have landed (in a normal run the dequant group has waited for all of them; after
-    // an abort it may not have, and no copy may still be writing when the CTA exits).
-    for (int s = 0; s < kStages && s < k; ++s) {
-      const int kl = s + ((k - 1 - s) / kStages) * kStages;  // last tile issued on stage s
-      mbar_wait(&bar_full[s], (uint32_t)(kl / kStages) & 1u, p.timeout_ns);
-    }
+    producer_warp(smem, p, it, bar_full, bar_empty, bar_qfree);
     return;
   }
 
