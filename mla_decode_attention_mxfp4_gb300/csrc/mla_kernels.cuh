@@ -769,6 +769,62 @@ __device__ __noinline__ void reference_warp(uint8_t* smem, uint64_t* bar_full, u
   }
 }
 
+// O^T rescale (out of line: it runs only when a running maximum or the tile reference
+// moves): column 8q + i of each block holds head (8q + i) % 16, scaled by alpha[head] * rs.
+__device__ __noinline__ void rescale_o(uint32_t t_lane, const float* alpha, float rs) {
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 4) {
+    const float4 a4 = *reinterpret_cast<const float4*>(alpha + i);
+    f[i] = a4.x * rs; f[i + 1] = a4.y * rs; f[i + 2] = a4.z * rs; f[i + 3] = a4.w * rs;
+  }
+#pragma unroll 1
+  for (int blk = 0; blk < 4; ++blk) {
+    const uint32_t col = t_lane + kColO + 32 * blk;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t a[8];
+      tmem_ld8_nowait(col + 8 * q, a);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = __float_as_uint(__uint_as_float(a[i]) * f[(8 * q + i) & 15]);
+      tmem_st8(col + 8 * q, a);
+    }
+  }
+  tc_wait_st();
+}
+
+// Segment output (out of line: it runs once per segment, apart from the per-tile code):
+// O^T of the thread's dims (t + 128 blk), times each head's factor, as bf16 output rows
+// (whole sequences) or fp32 partial rows.
+__device__ __noinline__ void segment_out(void* dst, bool whole, const float* ofac, uint32_t t_lane, int t) {
+  float of[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 4) {
+    const float4 f4 = *reinterpret_cast<const float4*>(ofac + i);
+    of[i] = f4.x; of[i + 1] = f4.y; of[i + 2] = f4.z; of[i + 3] = f4.w;
+  }
+#pragma unroll 1
+  for (int blk = 0; blk < 4; ++blk) {
+    uint32_t a[16], c[16];
+    const uint32_t col = t_lane + kColO + 32 * blk;
+    tmem_ld16_nowait(col, a);
+    tmem_ld16_nowait(col + 16, c);
+    tc_wait_ld();
+    const int dim = 128 * blk + t;
+    if (whole) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(dst) + dim;
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h)
+        o[h * kDv] = __float2bfloat16_rn(((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h]);
+    } else {
+      float* o = static_cast<float*>(dst) + dim;
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) o[h * kDv] = ((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h];
+    }
+  }
+}
+
 // Producer warp of mla_split_kernel, one thread (out of line, like the reference warp: its
 // code lies apart from the other roles').  It walks the tiles in the CTA's order and fills
 // stage k % kStages once the dequant group released it: packed rows and scale bytes by bulk
@@ -1242,24 +1298,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const __grid_con
       // ---- P.V of tile k-1 must be complete: O^T rescale and V^T below ----
       if (k > 0) wait_or_flag(&bar_pv[(k - 1) & 1], ((k - 1) >> 1) & 1, p, aborted);
       tc_fence_after();
-      if (resc) {
-        const float rs = exp2i(R - Rnew);
-        // eight columns at a time (column 8q + i holds head (8q + i) % 16): few live registers
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          const uint32_t col = t_lane + kColO + 32 * blk;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t a[8];
-            tmem_ld8_nowait(col + 8 * q, a);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = __float_as_uint(__uint_as_float(a[i]) * (alpha_v[(8 * q + i) & 15] * rs));
-            tmem_st8(col + 8 * q, a);
-          }
-        }
-        tc_wait_st();
-      }
+      if (resc) rescale_o(t_lane, mstate + kHeads, exp2i(R - Rnew));
       R = Rnew;
       // ---- V^T of tile k: this thread's token, all 512 dims, from the K tile in tensor memory ----
       {
@@ -1303,33 +1342,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const __grid_con
         named_sync(kBarSm, kSmThreads);
         wait_or_flag(&bar_pv[k & 1], (k >> 1) & 1, p, aborted);
         tc_fence_after();
-        float of[16];
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 f4 = *reinterpret_cast<const float4*>(ofac + i);
-          of[i] = f4.x; of[i + 1] = f4.y; of[i + 2] = f4.z; of[i + 3] = f4.w;
-        }
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t a[16], c[16];
-          const uint32_t col = t_lane + kColO + 32 * blk;
-          tmem_ld16_nowait(col, a);
-          tmem_ld16_nowait(col + 16, c);
-          tc_wait_ld();
-          const int dim = 128 * blk + t;
-          if (whole) {
-            __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
-#pragma unroll
-            for (int h = 0; h < kHeads; ++h)
-              o[h * kDv] =
-                  __float2bfloat16_rn(((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h]);
-          } else {
-            float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
-#pragma unroll
-            for (int h = 0; h < kHeads; ++h)
-              o[h * kDv] = ((__uint_as_float(a[h]) + __uint_as_float(c[h])) * kOutInv) * of[h];
-          }
-        }
+        segment_out(whole ? (void*)(p.out + (long long)it.b * kHeads * kDv)
+                          : (void*)(p.ws.part_acc + (long long)slot * kHeads * kDv),
+                    whole, ofac, t_lane, t);
         tc_fence_before();
         named_sync(kBarSm, kSmThreads);  // lw, ofac and the accumulator are reused by the next segment
       }
