@@ -39,11 +39,14 @@ constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kMmaWarp = 0, kProdWarp = 1, kSmWarp0 = 2;
 constexpr int kThreads = (2 + kSmWarps) * 32;
 
-// Tensor memory: S^T ring of two (32 columns each: hi query part 0..15, lo part 16..31), O^T
-// accumulator (4 blocks of 128 dims x 32 columns: P' hi part 0..15, lo part 16..31).
-constexpr uint32_t kTmemCols = 256;
+// Tensor memory: S^T ring of two (32 columns each: hi query part 0..15, lo part 16..31), two O^T
+// accumulators (segment j uses the one at kColO + kColsO (j & 1); each 4 blocks of 128 dims x 32
+// columns: P' hi part 0..15, lo part 16..31), so that a segment's output is read while the
+// next segment's P.V already accumulates.
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 64;
+constexpr uint32_t kColsO = 128;
 
 // Shared memory.
 constexpr int kOffStages = 0;                                      // boxes 1024-byte aligned
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
         for (int blk = 0; blk < kVBoxes; ++blk) {
           // V^T, MN-major, 128-byte swizzle: box blk holds dims 128 blk.., 32 tokens = 4 atoms
           const uint64_t da = smem_desc_sw128(st + blk * kBoxTileBytes + js * 32 * kBoxBytes, kBoxTileBytes, 1024);
-          umma_f8_ss_warp(tmem + kColO + 32 * blk, da, dp + (uint64_t)((js * 4 * kPtLbo) >> 4), idesc_pv,
+          umma_f8_ss_warp(tmem + kColO + kColsO * (cur.seg & 1) + 32 * blk, da, dp + (uint64_t)((js * 4 * kPtLbo) >> 4), idesc_pv,
                           (js > 0 || !seg_first) ? 1u : 0u);
         }
       umma_commit_warp(bar_pv);
@@ -254,6 +257,39 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
   const float kvs = *p.kv_scale;
   float ch[16];  // score factor of each head for the current segment: qch * kv_scale
   float l_part[16];
+  // a segment's output waits for the next tile (see the epilogue)
+  bool epi = false;
+  int epi_b = 0, epi_slot = 0, epi_par = 0;
+  bool epi_whole = false;
+  auto write_out = [&](int b, int slot, bool whole, int par) {
+    const float* ofac = reinterpret_cast<const float*>(smem + kOffMlast);
+    float of[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 f4 = *reinterpret_cast<const float4*>(ofac + i);
+      of[i] = f4.x; of[i + 1] = f4.y; of[i + 2] = f4.z; of[i + 3] = f4.w;
+    }
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      uint32_t a[16], c[16];
+      const uint32_t col = t_lane + kColO + kColsO * par + 32 * blk;
+      tmem_ld16_nowait(col, a);
+      tmem_ld16_nowait(col + 16, c);
+      tc_wait_ld();
+      const int dim = 128 * blk + t;
+      if (whole) {
+        __nv_bfloat16* o = p.out + (long long)b * kHeads * kDv + dim;
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h)
+          o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h]);
+      } else {
+        float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h];
+      }
+    }
+    tc_fence_before();
+  };
   int k = 0;
   bool has_next;
   do {
@@ -381,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
     if (resc) {
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
-        const uint32_t col = t_lane + kColO + 32 * blk;
+        const uint32_t col = t_lane + kColO + kColsO * (it.seg & 1) + 32 * blk;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           uint32_t a[8];
@@ -398,8 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_pready);
+    if (epi) {  // the previous segment's output (its last P.V, tile k - 1, was waited for above)
+      write_out(epi_b, epi_slot, epi_whole, epi_par);
+      epi = false;
+    }
     if (it.last) {
-      // ---- segment epilogue: O = (hi + lo) * kv_scale / l' ----
+      // ---- segment epilogue: O = (hi + lo) * kv_scale / l'; O^T is read at the next tile,
+      // after this segment's last P.V, while the next segment accumulates in the other O^T ----
       float* lw = reinterpret_cast<float*>(smem + kOffLw);
       float* ofac = reinterpret_cast<float*>(smem + kOffMlast);
       const float ls = warp_reduce16<false>(l_part, lane);
@@ -415,37 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_fp8_kernel(const __grid
         ofac[h] = kvs / L;
       }
       named_sync(kBarSm, kSmThreads);
-      wait_fp8(bar_pv, k & 1, p, aborted);
-      tc_fence_after();
-      float of[16];
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        const float4 f4 = *reinterpret_cast<const float4*>(ofac + i);
-        of[i] = f4.x; of[i + 1] = f4.y; of[i + 2] = f4.z; of[i + 3] = f4.w;
-      }
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t a[16], c[16];
-        const uint32_t col = t_lane + kColO + 32 * blk;
-        tmem_ld16_nowait(col, a);
-        tmem_ld16_nowait(col + 16, c);
-        tc_wait_ld();
-        const int dim = 128 * blk + t;
-        if (whole) {
-          __nv_bfloat16* o = p.out + (long long)it.b * kHeads * kDv + dim;
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h)
-            o[h * kDv] = __float2bfloat16_rn((__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h]);
-        } else {
-          float* o = p.ws.part_acc + (long long)slot * kHeads * kDv + dim;
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h) o[h * kDv] = (__uint_as_float(a[h]) + __uint_as_float(c[h])) * of[h];
-        }
-      }
-      tc_fence_before();
-      named_sync(kBarSm, kSmThreads);
+      epi = true;
+      epi_b = it.b;
+      epi_slot = slot;
+      epi_whole = whole;
+      epi_par = it.seg & 1;
     }
     has_next = it.next();
+    if (epi && !has_next) {  // the CTA's last segment: its output once its last P.V completed
+      wait_fp8(bar_pv, k & 1, p, aborted);
+      tc_fence_after();
+      write_out(epi_b, epi_slot, epi_whole, epi_par);
+      epi = false;
+    }
     ++k;
   } while (has_next);
   tc_fence_before();
