@@ -264,6 +264,29 @@ def test_ragged_edges(lens):
     check_close(as64(out), ref, str(lens[:8]))
 
 
+def _resident_ctas():
+    return torch.cuda.get_device_properties(0).multi_processor_count  # one split CTA per SM
+
+
+@pytest.mark.parametrize("case", ["tiles_below_grid", "tiles_at_grid", "tiles_above_grid",
+                                  "one_sequence_over_every_range", "one_sequence_one_tile_more"])
+def test_ranges_of_whole_tiles_at_the_grid_size(case):
+    # The partition gives each resident CTA floor(gT/G) .. floor((g+1)T/G) of the T tiles:
+    # T just below, at and just above G, and a single sequence split over every range (the
+    # merge then combines G partials, or G partials with one range holding two tiles).
+    G = _resident_ctas()
+    lens = {"tiles_below_grid": [128] * (G - 2) + [77],
+            "tiles_at_grid": [128] * G,
+            "tiles_above_grid": [128] * G + [3],
+            "one_sequence_over_every_range": [128 * G],
+            "one_sequence_one_tile_more": [128 * G + 5]}[case]
+    d = MI.make_custom(lens, seed=len(lens) + 7)
+    out, st = gpu_decode(d)
+    assert st == 0
+    ref = oracle.decode(d.q, d.kv_packed, d.kv_scale, d.kv_indptr, d.sm_scale)
+    check_close(as64(out), ref, case)
+
+
 def test_many_tiny_sequences():
     rng = np.random.default_rng(9)
     lens = rng.integers(0, 7, 700).tolist()
